@@ -1,0 +1,324 @@
+/*
+ * sds.h -- C ABI of the stream-batch diffusion hot path for B300 (sm_103a).
+ *
+ * One context (sds_ctx) serves S independent streams of one workload shape.
+ * Per step a caller typically issues, on one CUDA stream:
+ *
+ *   sds_kv_push      K2  RoPE the new chunk's keys, append K/V into the ring
+ *   sds_sink_refresh K3  fill empty sinks / refresh the least similar sink
+ *   sds_attend       K1  cross-frame softmax attention of all n slots' queries
+ *   sds_step_update  K4  R-CFG + stream-batch update (+ SSF, + motion EMA)
+ *
+ * Image batch mode (ring_R == 0) skips the first two: sds_attend then takes
+ * the caller's concatenated batch K/V.
+ *
+ * Common rules for every call below.
+ *  - Pointers named "device" are CUDA device (or managed) pointers into
+ *    memory the caller owns; the library never frees or retains them past
+ *    the call's stream work.  Tensors are dense, row-major, without padding.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns; fp32 tensors are float.
+ *  - Device pointers must be 16-byte aligned; element counts that feed a
+ *    vectorised kernel must be multiples of 4 (checked, see each call).
+ *  - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns without synchronising, except
+ *    sds_read_state.  Host-side metadata (frame counter, RoPE offset, ring
+ *    head) advances when a call is enqueued, so calls on one context must
+ *    be issued in order on one stream.
+ *  - Decisions the kernels take (skip flag, refreshed sink, noise rate) stay
+ *    in device memory; sds_read_state copies them out.
+ *  - Arguments are validated on the host before any launch.  A failed call
+ *    returns a status, changes no state and launches nothing;
+ *    sds_last_error() then describes it.  CUDA launch failures map to
+ *    SDS_ERR_CUDA.  Nothing aborts the process, traps or waits without bound
+ *    on the device: a kernel that meets an impossible condition records it
+ *    in the per-stream error word (sds_stream_state.error_word) and returns.
+ *  - A context is not thread safe; use one per host thread.
+ *
+ * Citations name the page and the passage that define each operation:
+ *  [SD]  "StreamDiffusion: A Pipeline-level Solution for Real-time
+ *        Interactive Generation" (ICCV 2025 paper notes), sections
+ *        "Stream Batch", "Residual CFG (R-CFG)", "Stochastic Similarity
+ *        Filter (SSF)".
+ *  [SDO] "StreamDiffusion complete analysis" (overview page), "Core
+ *        features" and "Technical highlights" (cfg_type, max_skip_frame).
+ *  [V2]  StreamDiffusionV2 summary page, "Adaptive sink and RoPE refresh",
+ *        "Motion-aware noise scheduler", "SLO-aware batching scheduler".
+ *  [BLOG] StreamDiffusion blog (mpbf.cn), section 7, the DDPM ancestral step.
+ */
+#ifndef SDS_H
+#define SDS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SDS_API __attribute__((visibility("default")))
+#else
+#define SDS_API
+#endif
+
+#define SDS_ABI_VERSION 1
+#define SDS_MAX_SLOTS 8
+#define SDS_MAX_CHUNK_FRAMES 8
+
+typedef struct sds_ctx sds_ctx;
+typedef void* sds_stream_t; /* cudaStream_t */
+
+typedef enum {
+  SDS_OK = 0,
+  SDS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or config field */
+  SDS_ERR_OOM = 2,         /* device allocation failed or exceeds mem_cap_bytes */
+  SDS_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+  SDS_ERR_STATE = 4,       /* call out of order (e.g. attend before any push) */
+  SDS_ERR_UNSUPPORTED = 5  /* valid request this build does not implement */
+} sds_status;
+
+/*
+ * Workload description, copied at sds_create.  All integers are int64 and
+ * all reals double so the struct has no padding.
+ *
+ * Geometry: streams S; slots_n = n denoise slots of the stream batch
+ * ([SD] "Stream Batch": n steps of n different frames form one batch);
+ * frames_T frames per chunk; tokens_L tokens per frame; heads_H x head_dim
+ * (head_dim 64 or 128); sink_M sink frames and ring_R rolling frames of
+ * cached K/V ([V2] sink tokens + rolling KV cache).  ring_R == 0 selects
+ * image batch mode: no ring, no RoPE, and sds_attend takes external K/V.
+ *
+ * RoPE: rope_on, token grid grid_h x grid_w (grid_h*grid_w == tokens_L),
+ * rope_base, and rope_tau: when the next chunk's start position, counted
+ * from the last reset, exceeds rope_tau the phase is reset ([V2] "reset the
+ * RoPE phase when the frame index exceeds a threshold").  The head dim is
+ * split into temporal/row/column segments d_t, d_y, d_x with
+ * d_y = d_x = 2*floor(head_dim/6), d_t = head_dim - 2*d_y; pair (2i, 2i+1)
+ * of a segment of width w turns by pos * rope_base^(-2i/w).
+ *
+ * Sink refresh ([V2]): emb_dim_D-dimensional chunk embeddings, threshold s_th.
+ *
+ * Schedule ([SD] R-CFG, [BLOG]): num_train_steps betas, scaled linear from
+ * beta_start to beta_end; slot i runs at timestep
+ * (num_train_steps-1) - t_index[i]*(num_train_steps/num_inference_steps).
+ * cfg_type: 0 = no guidance (eps_cfg = eps_c), 1 = self-negative R-CFG with
+ * gamma, delta ([SDO] cfg_type="self").
+ *
+ * slot_elems: fp32 elements of one slot latent (T * frame_elems in video).
+ * SSF ([SD] SSF, [SDO]): ssf_elems per frame, ssf_eta, max_skip_frame.
+ * Motion ([V2]): frame_elems per latent frame, window mot_k, mot_sigma,
+ * mot_lambda, noise-rate bounds s_min <= s_max.
+ *
+ * mem_cap_bytes: if nonzero, sds_create fails with SDS_ERR_OOM when the
+ * context's device memory would exceed it (no allocation is attempted).
+ */
+typedef struct {
+  int64_t abi_version; /* must equal SDS_ABI_VERSION */
+  int64_t streams, slots_n, frames_T, tokens_L, heads_H, head_dim, sink_M, ring_R;
+  int64_t rope_on, grid_h, grid_w, rope_tau;
+  int64_t emb_dim_D;
+  int64_t t_index[SDS_MAX_SLOTS];
+  int64_t num_inference_steps, num_train_steps, cfg_type;
+  int64_t slot_elems;
+  int64_t ssf_on, ssf_elems, max_skip_frame;
+  int64_t motion_on, frame_elems, mot_k;
+  int64_t mem_cap_bytes;
+  double rope_base, s_th, beta_start, beta_end, gamma, delta, ssf_eta;
+  double mot_sigma, mot_lambda, s_min, s_max;
+} sds_config;
+
+/*
+ * Inputs and outputs of one stream-batch update (sds_step_update).  Every
+ * array is fp32, device, [S][slot_elems] (stream-major) unless stated.
+ *   x[i]      slot i's current latent x_{t_i}, i < n
+ *   x0[i]     slot i's own input-frame latent (the R-CFG x0)
+ *   eps_c[i]  the model's conditional noise prediction for slot i
+ *   z[i]      ancestral noise that re-noises slot i's prediction to slot
+ *             i+1's level, i < n-1
+ *   x_next[i] next step's latents: x_next[0] is the incoming frame noised to
+ *             slot 0's level; x_next[i+1] comes from slot i.  x_next[i] may
+ *             alias x[i] (in-place update is safe).
+ *   out       the completed frame: slot n-1's predicted x0
+ *   x0_new, eps_new  the incoming frame's latent and its noise
+ *   ssf_frame [S][ssf_elems] or NULL: run the similarity filter on this
+ *             frame in the same pass; ssf_u [S] uniform draws in [0,1)
+ *   motion_chunk [S][frames_T][frame_elems] or NULL: update the motion
+ *             estimate and noise rate from these latent frames
+ * x0 shifting between steps (slot i+1's x0 is this step's x0[i]) is left to
+ * the caller, which can rotate the pointers at no cost.
+ */
+typedef struct {
+  const float* x[SDS_MAX_SLOTS];
+  const float* x0[SDS_MAX_SLOTS];
+  const float* eps_c[SDS_MAX_SLOTS];
+  const float* z[SDS_MAX_SLOTS];
+  float* x_next[SDS_MAX_SLOTS];
+  float* out;
+  const float* x0_new;
+  const float* eps_new;
+  const float* ssf_frame;
+  const float* ssf_u;
+  const float* motion_chunk;
+} sds_step_io;
+
+/* Per-stream decisions, as of the last completed call that made them. */
+typedef struct {
+  int64_t ssf_evals;      /* frames the filter has seen */
+  int64_t ssf_skip;       /* last frame skipped (1) or processed (0) */
+  int64_t ssf_skip_count; /* consecutive skips so far */
+  int64_t ssf_has_ref;    /* a reference frame exists */
+  double ssf_cos;         /* cosine of the last frame vs the reference */
+  double ssf_p;           /* its skip probability */
+  int64_t sink_j;         /* last refresh: chosen sink (-1 if none) */
+  int64_t sink_fire;      /* 0 kept, 1 replaced, 2 filled an empty sink */
+  double sink_alpha_min;  /* smallest cosine of the last refresh test */
+  double sink_alpha_2;    /* second smallest (+inf if M == 1) */
+  int64_t motion_pairs;   /* motion values measured so far */
+  double motion_dhat;     /* last normalised, clipped motion */
+  double noise_rate;      /* EMA noise rate s */
+  double motion_d[SDS_MAX_CHUNK_FRAMES]; /* last chunk's pair motions (NaN if absent) */
+  int64_t error_word;     /* nonzero: a kernel met an impossible condition */
+} sds_stream_state;
+
+/* Host-side ring metadata (identical for all streams of a context). */
+typedef struct {
+  int64_t frames_pushed; /* F */
+  int64_t rope_offset;   /* o: positions count from frame o */
+  int64_t chunk_p0;      /* start position of the last pushed chunk */
+  int64_t ring_valid;    /* min(F, R) */
+  int64_t sinks_filled;
+  int64_t rope_resets;
+  int64_t chunks;
+} sds_meta;
+
+/* Device buffers owned by the context, valid until sds_destroy. */
+typedef struct {
+  void* kv_k;      /* bf16 [S][(M+R)*L][H][d]: sink frames, then ring frames */
+  void* kv_v;      /* same layout */
+  float* sink_emb; /* fp32 [S][M][D] */
+  int64_t kv_rows; /* (M+R)*L */
+} sds_buffers;
+
+/* ABI version the library was built with (SDS_ABI_VERSION). */
+SDS_API int sds_abi_version(void);
+
+/*
+ * Validate cfg, allocate the context's device buffers (K/V ring and sinks,
+ * sink embeddings, RoPE cos/sin table, schedule coefficients, SSF reference
+ * frames, motion previous frames, decision state, reduction scratch) on the
+ * current CUDA device, zero them, and return the context in *out.
+ * No allocation happens after this call.
+ * Errors: SDS_ERR_INVALID_ARG (cfg), SDS_ERR_OOM, SDS_ERR_CUDA.  On error
+ * *out is NULL and sds_last_error(NULL) describes the failure.
+ */
+SDS_API sds_status sds_create(const sds_config* cfg, sds_ctx** out);
+
+/* Free the context and its device buffers (synchronises the device). */
+SDS_API void sds_destroy(sds_ctx* ctx);
+
+/* Description of the last error on ctx (ctx == NULL: the last failed create
+ * on this thread).  The string is owned by the library. */
+SDS_API const char* sds_last_error(const sds_ctx* ctx);
+
+/*
+ * K2 -- ring append with RoPE ([V2] rolling KV cache; "Adaptive sink and
+ * RoPE refresh").  k, v: device bf16 [S][T*L][H][d], the new chunk's keys
+ * and values.  Computes the chunk start position p0 = F - o (reset: if
+ * p0 > rope_tau then o = F, p0 = 0), rotates each key of frame j, token
+ * (y, x) at positions (p0 + j, y, x) in fp32 and stores it as bf16; copies
+ * the values; frame F + j goes to ring slot (F + j) mod R, overwriting the
+ * oldest frame.  Then F += T.
+ * Errors: SDS_ERR_STATE in image mode; SDS_ERR_INVALID_ARG for NULL or
+ * misaligned pointers.
+ */
+SDS_API sds_status sds_kv_push(sds_ctx* ctx, const void* k, const void* v, sds_stream_t stream);
+
+/*
+ * K3 -- adaptive sink refresh ([V2] "Adaptive sink and RoPE refresh": the
+ * least similar sink is refreshed when the cosine of the new chunk embedding
+ * to it falls below s_th).  chunk_emb: device fp32 [S][D].
+ * While sinks are empty, they are filled in index order from frames 0, 1, ..
+ * of the chunk just pushed, and take chunk_emb as their embedding.  Once
+ * full: alpha_j = cos(h, e_j) in double, j* = argmin (lowest index on
+ * ties); if alpha_{j*} < s_th, sink j*'s K/V become frame 0 of the chunk
+ * just pushed (already rotated) and e_{j*} = h.  The decision is taken on
+ * the device; nothing is read back.  No-op when sink_M == 0.
+ * Errors: SDS_ERR_STATE before the first push or in image mode.
+ */
+SDS_API sds_status sds_sink_refresh(sds_ctx* ctx, const float* chunk_emb, sds_stream_t stream);
+
+/*
+ * K1 -- cross-frame attention ([SD] "Stream Batch": Attn(Q_{t,i}, K_Batch,
+ * V_Batch) = Softmax(Q K_Batch^T / sqrt(d)) V_Batch).
+ * q: device bf16 [S][n*T*L][H][d] (video) or [S][n*L][H][d] (image): the
+ * queries of all n slots, stacked.  o: device bf16, same shape as q.
+ * Video mode (ext_k == ext_v == NULL): every query row of the last pushed
+ * chunk is rotated at (p0 + j, y, x) (all slots share the chunk's
+ * positions), then attends to all valid keys: the filled sinks and the
+ * filled ring frames (including the chunk just pushed); no causal mask.
+ * Image mode: ext_k, ext_v device bf16 [S][n*L][H][d], the batch K/V; no
+ * RoPE.  Softmax in fp32 with bf16 tensor-core products, output rounded
+ * to bf16.
+ * Errors: SDS_ERR_STATE (video mode before any push); SDS_ERR_INVALID_ARG.
+ */
+SDS_API sds_status sds_attend(sds_ctx* ctx, const void* q, void* o, const void* ext_k,
+                      const void* ext_v, sds_stream_t stream);
+
+/*
+ * Context-free attention: o = Softmax(q k^T / sqrt(d)) v for each of S
+ * independent problems, q/o device bf16 [S][Lq][H][d], k/v device bf16
+ * [S][Lk][H][d], head_dim 64 or 128, no RoPE ([SD] cross-frame attention
+ * equation).  Lq >= 1, Lk >= 1.
+ */
+SDS_API sds_status sds_attention(const void* q, const void* k, const void* v, void* o, int64_t S,
+                         int64_t Lq, int64_t Lk, int64_t H, int64_t head_dim,
+                         sds_stream_t stream);
+
+/*
+ * K4 -- one fused pass ([SD] "Residual CFG", [BLOG] update, [SD] "SSF",
+ * [V2] "Motion-aware noise scheduler").  Per slot i, with a = alphabar of
+ * slot i's timestep, in fp32 with host-double coefficients:
+ *   eps_neg = (x_i - sqrt(a) x0_i) / sqrt(1 - a)
+ *   eps_cfg = gamma eps_c + delta (1 - gamma) eps_neg   (= the printed
+ *             delta eps_neg + gamma (eps_c - delta eps_neg))
+ *   x0hat   = (x_i - sqrt(1 - a) eps_cfg) / sqrt(a)
+ *   x_next[i+1] = sqrt(a_{i+1}) x0hat + sqrt(1 - a_{i+1}) z_i  (i < n-1)
+ *   out = x0hat of slot n-1;  x_next[0] = sqrt(a_0) x0_new + sqrt(1-a_0) eps_new.
+ * With io->ssf_frame: the similarity filter of sds_ssf on that frame.
+ * With io->motion_chunk: per frame pair the RMS difference d (the previous
+ * chunk's last frame pairs with frame 0); dhat = min(1, max of the last
+ * mot_k values / mot_sigma); target = s_min + (s_max - s_min) dhat;
+ * s <- s + (1 - mot_lambda)(target - s); s starts at s_min.
+ * Reductions are deterministic (fixed order, fp32 within a thread, double
+ * beyond), finished by the last block of the launch.
+ * Errors: SDS_ERR_INVALID_ARG (NULL/misaligned arrays, ssf/motion requested
+ * but disabled in the config, sizes not multiples of 4).
+ */
+SDS_API sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t stream);
+
+/*
+ * K4, filter only ([SD] "SSF": P(skip) = max{0, (S_C(I_t, I_ref) - eta) /
+ * (1 - eta)} with the cosine S_C, sampled not thresholded; [SDO] at most
+ * max_skip_frame consecutive skips).  frame: device fp32 [S][ssf_elems];
+ * u: device fp32 [S], uniform draws in [0,1).  Per stream: the first frame
+ * is processed; then c = cos(I, I_ref) (0 if a norm is 0), P = min(1,
+ * max(0, (c - eta)/(1 - eta))), skip = (u < P) and (skip_count <
+ * max_skip_frame).  A processed frame becomes the reference.
+ */
+SDS_API sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds_stream_t stream);
+
+/* Synchronise `stream` and copy the S per-stream decision records to host
+ * memory out[0..S-1]. */
+SDS_API sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream);
+
+/* Host-side ring metadata (no device access). */
+SDS_API sds_status sds_get_meta(const sds_ctx* ctx, sds_meta* out);
+
+/* Device buffers owned by the context (for inspection and checkpoints). */
+SDS_API sds_status sds_get_buffers(const sds_ctx* ctx, sds_buffers* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDS_H */

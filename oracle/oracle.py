@@ -220,13 +220,14 @@ class Stream:
         lib().orc_rotate_queries(self.h, _p(q), _p(out))
         return out
 
-    def attend(self, qrot: np.ndarray, rows=None) -> np.ndarray:
-        qrot = np.ascontiguousarray(qrot, dtype=np.uint16)
+    def attend(self, q: np.ndarray, rows=None) -> np.ndarray:
+        """Attention of (unrotated) query rows [n*T*L][H][d]; rotation happens inside."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
         w = self.w
-        nrow = qrot.shape[0]
+        nrow = q.shape[0]
         rows = np.arange(nrow, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
         out = np.zeros((len(rows), w["H"], w["d"]), dtype=np.float64)
-        lib().orc_attend(self.h, _p(qrot), _p(rows), len(rows), _p(out))
+        lib().orc_attend(self.h, _p(q), _p(rows), len(rows), _p(out))
         return out
 
     def step_update(self, x, x0, eps_c, z, x0_new, eps_new):

@@ -460,20 +460,32 @@ void orc_rotate_queries(void* p, const uint16_t* q, uint16_t* qrot) {
   }
 }
 
-// a4 (video mode): attention of selected rows of the rotated queries against
-// the stream's sink + ring keys.  qrot: output of orc_rotate_queries.
-void orc_attend(void* p, const uint16_t* qrot, const long long* rows, long long nsel, double* out) {
+// a4 (video mode): attention of selected query rows against the stream's
+// sink + ring keys.  q: bf16 [n*T*L][H][d] as given (unrotated); each
+// selected row is rotated at its chunk position (O2) and rounded to bf16 --
+// the operand the tensor cores consume -- before the scores are formed.
+void orc_attend(void* p, const uint16_t* q, const long long* rows, long long nsel, double* out) {
   Stream* s = (Stream*)p;
   const orc_cfg& c = s->c;
   long long nk = orc_key_rows(p, nullptr);
   std::vector<long long> key_rows((size_t)nk);
   orc_key_rows(p, key_rows.data());
+  long long TL = c.T * c.L;
 #pragma omp parallel for schedule(dynamic, 1) collapse(2)
   for (long long r = 0; r < nsel; ++r) {
     for (long long h = 0; h < c.H; ++h) {
-      std::vector<double> qd((size_t)c.d);
-      const uint16_t* qr = qrot + (size_t)(rows[r] * c.H * c.d + h * c.d);
-      for (long long t = 0; t < c.d; ++t) qd[(size_t)t] = bf16_to_double(qr[t]);
+      std::vector<double> in((size_t)c.d), qd((size_t)c.d);
+      const uint16_t* qr = q + (size_t)(rows[r] * c.H * c.d + h * c.d);
+      for (long long t = 0; t < c.d; ++t) in[(size_t)t] = bf16_to_double(qr[t]);
+      if (c.rope_on) {
+        long long tok = rows[r] % TL;
+        long long j = tok / c.L, l = tok % c.L;
+        long long pos[3] = {s->p0 + j, l / c.grid_w, l % c.grid_w};
+        rope_rotate(in.data(), qd.data(), c.d, pos, c.rope_base);
+        for (long long t = 0; t < c.d; ++t) qd[(size_t)t] = bf16_to_double(double_to_bf16(qd[(size_t)t]));
+      } else {
+        qd = in;
+      }
       attend_row(qd.data(), s->kbuf.data(), s->vbuf.data(), key_rows, c.H, h, c.d,
                  out + (size_t)((r * c.H + h) * c.d));
     }

@@ -1,0 +1,648 @@
+// sds_api.cu -- host side of the C ABI declared in include/sds.h:
+// validation, device buffers, host ring metadata, RoPE and schedule tables,
+// and kernel launches.  No compute happens here; every step of the path runs
+// in the kernels of k_attn.cu, k_ring.cu and k_step.cu.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "sds_internal.h"
+
+using namespace sds;
+
+struct sds_ctx {
+  sds_config cfg;
+  int device = 0;
+  int sm_count = 0;
+  bool image_mode = false;
+  // device buffers (owned)
+  uint16_t* kv_k = nullptr;
+  uint16_t* kv_v = nullptr;
+  float* sink_emb = nullptr;
+  float2* rope_tab = nullptr;
+  float* ssf_ref = nullptr;   // [2][S][E]
+  float* mot_prev = nullptr;  // [2][S][N_f]
+  DevState* state = nullptr;  // [S]
+  double* partials = nullptr;
+  unsigned int* counters = nullptr;  // [1 + S]
+  std::vector<void*> allocs;
+  // tables
+  int rope_seg[3] = {0, 0, 0};
+  int tab_off[3] = {0, 0, 0};
+  int tab_rows_t = 0;
+  double abar_slot[SDS_MAX_SLOTS] = {};
+  // host ring metadata
+  int64_t F = 0, o = 0, p0 = 0, chunk_first = -1, sinks_filled = 0, resets = 0, chunks = 0;
+  int64_t motion_calls = 0;
+  int64_t nb_u = 0, nb_s = 0, nb_m = 0;
+  CUtensorMap tm_kv_k, tm_kv_v;
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+sds_status fail(sds_ctx* c, sds_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) {
+    c->err = buf;
+  } else {
+    g_create_err = buf;
+  }
+  return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// scaled-linear betas; alphabar_t = prod_{s<=t} (1 - beta_s)
+void alpha_bar(const sds_config& c, std::vector<double>& out) {
+  out.resize((size_t)c.num_train_steps);
+  const double a = std::sqrt(c.beta_start), b = std::sqrt(c.beta_end);
+  double prod = 1.0;
+  for (int64_t t = 0; t < c.num_train_steps; ++t) {
+    const double r = a + (b - a) * (double)t / (double)(c.num_train_steps - 1);
+    prod *= 1.0 - r * r;
+    out[(size_t)t] = prod;
+  }
+}
+
+sds_status validate(const sds_config* c, std::string& why) {
+  auto bad = [&](const char* m) {
+    why = m;
+    return SDS_ERR_INVALID_ARG;
+  };
+  if (!c) return bad("config is NULL");
+  if (c->abi_version != SDS_ABI_VERSION) return bad("abi_version mismatch");
+  if (c->streams < 1 || c->streams > 65535) return bad("streams must be in [1, 65535]");
+  if (c->slots_n < 1 || c->slots_n > SDS_MAX_SLOTS) return bad("slots_n must be in [1, 8]");
+  if (c->heads_H < 1 || c->heads_H > 65535) return bad("heads_H must be in [1, 65535]");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c->tokens_L < 1) return bad("tokens_L must be >= 1");
+  if (c->frames_T < 1 || c->frames_T > SDS_MAX_CHUNK_FRAMES) return bad("frames_T must be in [1, 8]");
+  const bool image = c->ring_R == 0;
+  if (c->ring_R < 0 || c->sink_M < 0) return bad("ring_R and sink_M must be >= 0");
+  if (!image) {
+    if (c->ring_R < c->frames_T) return bad("ring_R must hold at least one chunk (ring_R >= frames_T)");
+    if (c->rope_on) {
+      if (c->grid_h < 1 || c->grid_w < 1 || c->grid_h * c->grid_w != c->tokens_L)
+        return bad("grid_h * grid_w must equal tokens_L");
+      if (c->rope_tau < 0 || c->rope_tau > (1 << 20)) return bad("rope_tau must be in [0, 2^20]");
+      if (!(c->rope_base > 1.0)) return bad("rope_base must be > 1");
+    }
+    if (c->sink_M > 0 && (c->emb_dim_D < 1 || c->emb_dim_D > (1 << 24)))
+      return bad("emb_dim_D must be >= 1 when sink_M > 0");
+    int64_t keys = (c->sink_M + c->ring_R) * c->tokens_L;
+    if (keys > (1ll << 30)) return bad("key buffer rows exceed 2^30");
+  } else {
+    if (c->frames_T != 1) return bad("image mode (ring_R == 0) needs frames_T == 1");
+    if (c->sink_M != 0) return bad("image mode (ring_R == 0) has no sinks");
+  }
+  if (c->num_train_steps < 2 || c->num_inference_steps < 1 ||
+      c->num_inference_steps > c->num_train_steps)
+    return bad("need 2 <= num_train_steps and 1 <= num_inference_steps <= num_train_steps");
+  if (!(c->beta_start > 0.0 && c->beta_end > 0.0 && c->beta_start < 1.0 && c->beta_end < 1.0))
+    return bad("betas must be in (0, 1)");
+  for (int64_t i = 0; i < c->slots_n; ++i) {
+    int64_t t = (c->num_train_steps - 1) -
+                c->t_index[i] * (c->num_train_steps / c->num_inference_steps);
+    if (c->t_index[i] < 0 || t < 0 || t >= c->num_train_steps)
+      return bad("t_index entry maps outside the training schedule");
+  }
+  if (c->cfg_type != 0 && c->cfg_type != 1) return bad("cfg_type must be 0 (none) or 1 (self)");
+  if (c->slot_elems < 4 || c->slot_elems % 4 != 0) return bad("slot_elems must be a positive multiple of 4");
+  if (c->ssf_on) {
+    if (c->ssf_elems < 4 || c->ssf_elems % 4 != 0) return bad("ssf_elems must be a positive multiple of 4");
+    if (!(c->ssf_eta < 1.0)) return bad("ssf_eta must be < 1");
+    if (c->max_skip_frame < 0) return bad("max_skip_frame must be >= 0");
+  }
+  if (c->motion_on) {
+    if (c->frame_elems < 4 || c->frame_elems % 4 != 0) return bad("frame_elems must be a positive multiple of 4");
+    if (c->mot_k < 1 || c->mot_k > kMaxMotionWindow) return bad("mot_k must be in [1, 64]");
+    if (!(c->mot_sigma > 0.0)) return bad("mot_sigma must be > 0");
+    if (!(c->s_min <= c->s_max)) return bad("s_min must be <= s_max");
+  }
+  return SDS_OK;
+}
+
+sds_status dev_alloc(sds_ctx* c, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(nullptr, SDS_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  c->allocs.push_back(*p);
+  e = cudaMemset(*p, 0, bytes);
+  if (e != cudaSuccess) return fail(nullptr, SDS_ERR_CUDA, "cudaMemset failed: %s", cudaGetErrorString(e));
+  return SDS_OK;
+}
+
+void free_all(sds_ctx* c) {
+  for (void* p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+}
+
+sds_status cuda_fail(sds_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, SDS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+void fill_attn_rope(const sds_ctx* c, AttnParams& ap) {
+  ap.rope_on = (int)(c->cfg.rope_on && !c->image_mode);
+  ap.p0 = (int)c->p0;
+  ap.tokens_L = (int)c->cfg.tokens_L;
+  ap.grid_w = (int)(c->cfg.grid_w > 0 ? c->cfg.grid_w : 1);
+  ap.chunk_tokens = (int)(c->cfg.frames_T * c->cfg.tokens_L);
+  for (int a = 0; a < 3; ++a) {
+    ap.rope_seg[a] = c->rope_seg[a];
+    ap.tab_off[a] = c->tab_off[a];
+  }
+  ap.rope_tab = c->rope_tab;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sds_abi_version(void) { return SDS_ABI_VERSION; }
+
+const char* sds_last_error(const sds_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_create_err.c_str();
+}
+
+sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
+  if (!out) return fail(nullptr, SDS_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  sds_status st = validate(cfg, why);
+  if (st != SDS_OK) return fail(nullptr, st, "invalid config: %s", why.c_str());
+  const sds_config& c = *cfg;
+  const int64_t S = c.streams, L = c.tokens_L, HD = c.heads_H * c.head_dim;
+  const bool image = c.ring_R == 0;
+
+  // sizes
+  const int64_t kv_elems = image ? 0 : S * (c.sink_M + c.ring_R) * L * HD;
+  const int64_t emb = image ? 0 : S * c.sink_M * (c.emb_dim_D > 0 ? c.emb_dim_D : 0);
+  int seg[3] = {0, 0, 0};
+  int64_t tab_entries = 0;
+  int tab_off[3] = {0, 0, 0};
+  int tab_rows_t = 0;
+  if (!image && c.rope_on) {
+    const int dy = 2 * (int)(c.head_dim / 6);
+    seg[0] = (int)c.head_dim - 2 * dy;
+    seg[1] = dy;
+    seg[2] = dy;
+    tab_rows_t = (int)(c.rope_tau + c.frames_T);
+    const int rows[3] = {tab_rows_t, (int)c.grid_h, (int)c.grid_w};
+    for (int a = 0; a < 3; ++a) {
+      tab_off[a] = (int)tab_entries;
+      tab_entries += (int64_t)rows[a] * (seg[a] / 2);
+    }
+  }
+  const int64_t nb_u = cdiv(c.slot_elems, kStepBlockElems);
+  const int64_t nb_s = c.ssf_on ? cdiv(c.ssf_elems, kStepBlockElems) : 0;
+  const int64_t nb_m = c.motion_on ? cdiv(c.frame_elems, kStepBlockElems) : 0;
+  const int64_t ssf_ref = c.ssf_on ? 2 * S * c.ssf_elems : 0;
+  const int64_t mot_prev = c.motion_on ? 2 * S * c.frame_elems : 0;
+  const int64_t partials = S * nb_s * 3 + S * c.frames_T * nb_m;
+  const size_t bytes = (size_t)kv_elems * 2 * 2 + (size_t)emb * 4 + (size_t)tab_entries * 8 +
+                       (size_t)ssf_ref * 4 + (size_t)mot_prev * 4 + (size_t)S * sizeof(DevState) +
+                       (size_t)partials * 8 + (size_t)(S + 1) * 4;
+  if (c.mem_cap_bytes > 0 && bytes > (size_t)c.mem_cap_bytes)
+    return fail(nullptr, SDS_ERR_OOM, "context needs %zu bytes > mem_cap_bytes %lld", bytes,
+                (long long)c.mem_cap_bytes);
+
+  sds_ctx* ctx = new sds_ctx();
+  ctx->cfg = c;
+  ctx->image_mode = image;
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (e != cudaSuccess) {
+    delete ctx;
+    cudaGetLastError();
+    return fail(nullptr, SDS_ERR_CUDA, "no usable CUDA device: %s", cudaGetErrorString(e));
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+  if (major != 10 || minor != 3) {
+    delete ctx;
+    return fail(nullptr, SDS_ERR_UNSUPPORTED, "this build targets sm_103a; device is sm_%d%d", major, minor);
+  }
+  for (int a = 0; a < 3; ++a) {
+    ctx->rope_seg[a] = seg[a];
+    ctx->tab_off[a] = tab_off[a];
+  }
+  ctx->tab_rows_t = tab_rows_t;
+  ctx->nb_u = nb_u;
+  ctx->nb_s = nb_s;
+  ctx->nb_m = nb_m;
+
+#define ALLOC(ptr, n)                                                         \
+  do {                                                                        \
+    void* tmp_ = nullptr;                                                     \
+    sds_status s_ = dev_alloc(ctx, &tmp_, (size_t)(n));                        \
+    if (s_ != SDS_OK) {                                                       \
+      free_all(ctx);                                                          \
+      delete ctx;                                                             \
+      return s_;                                                              \
+    }                                                                         \
+    ptr = reinterpret_cast<decltype(ptr)>(tmp_);                              \
+  } while (0)
+
+  ALLOC(ctx->kv_k, kv_elems * 2);
+  ALLOC(ctx->kv_v, kv_elems * 2);
+  ALLOC(ctx->sink_emb, emb * 4);
+  ALLOC(ctx->rope_tab, tab_entries * 8);
+  ALLOC(ctx->ssf_ref, ssf_ref * 4);
+  ALLOC(ctx->mot_prev, mot_prev * 4);
+  ALLOC(ctx->state, S * (int64_t)sizeof(DevState));
+  ALLOC(ctx->partials, partials * 8);
+  ALLOC(ctx->counters, (S + 1) * 4);
+#undef ALLOC
+
+  // RoPE table: angle pos * base^(-2i/w) in double, stored as fp32 (cos, sin)
+  if (tab_entries > 0) {
+    std::vector<float2> tab((size_t)tab_entries);
+    const int rows[3] = {tab_rows_t, (int)c.grid_h, (int)c.grid_w};
+    for (int a = 0; a < 3; ++a) {
+      const int half = seg[a] / 2;
+      for (int pos = 0; pos < rows[a]; ++pos)
+        for (int i = 0; i < half; ++i) {
+          const double th = (double)pos * std::pow(c.rope_base, -2.0 * i / (double)seg[a]);
+          tab[(size_t)tab_off[a] + (size_t)pos * half + i] = make_float2((float)std::cos(th), (float)std::sin(th));
+        }
+    }
+    e = cudaMemcpy(ctx->rope_tab, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      free_all(ctx);
+      delete ctx;
+      return fail(nullptr, SDS_ERR_CUDA, "table upload failed: %s", cudaGetErrorString(e));
+    }
+  }
+  // initial decision records
+  {
+    std::vector<DevState> st0((size_t)S);
+    for (auto& d : st0) {
+      std::memset(&d, 0, sizeof d);
+      d.pub.sink_j = -1;
+      d.pub.noise_rate = c.s_min;
+      d.pub.sink_alpha_min = INFINITY;
+      d.pub.sink_alpha_2 = INFINITY;
+      for (double& v : d.pub.motion_d) v = NAN;
+    }
+    e = cudaMemcpy(ctx->state, st0.data(), st0.size() * sizeof(DevState), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      free_all(ctx);
+      delete ctx;
+      return fail(nullptr, SDS_ERR_CUDA, "state upload failed: %s", cudaGetErrorString(e));
+    }
+  }
+  // schedule coefficients of the slots
+  {
+    std::vector<double> ab;
+    alpha_bar(c, ab);
+    for (int64_t i = 0; i < c.slots_n; ++i) {
+      const int64_t t = (c.num_train_steps - 1) - c.t_index[i] * (c.num_train_steps / c.num_inference_steps);
+      ctx->abar_slot[i] = ab[(size_t)t];
+    }
+  }
+  if (!image) {
+    const int64_t rows = (c.sink_M + c.ring_R) * L;
+    if (!make_tmap_bf16(&ctx->tm_kv_k, ctx->kv_k, HD, rows, S) ||
+        !make_tmap_bf16(&ctx->tm_kv_v, ctx->kv_v, HD, rows, S)) {
+      free_all(ctx);
+      delete ctx;
+      return fail(nullptr, SDS_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V ring");
+    }
+  }
+  *out = ctx;
+  return SDS_OK;
+}
+
+void sds_destroy(sds_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  free_all(ctx);
+  delete ctx;
+}
+
+sds_status sds_kv_push(sds_ctx* ctx, const void* k, const void* v, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (ctx->image_mode) return fail(ctx, SDS_ERR_STATE, "kv_push: context is in image batch mode");
+  if (!k || !v || !aligned16(k) || !aligned16(v))
+    return fail(ctx, SDS_ERR_INVALID_ARG, "kv_push: k and v must be non-NULL 16-byte aligned device pointers");
+  const sds_config& c = ctx->cfg;
+  int64_t p0 = ctx->F - ctx->o;
+  int64_t o = ctx->o;
+  bool reset = false;
+  if (p0 > c.rope_tau) {
+    o = ctx->F;
+    p0 = 0;
+    reset = true;
+  }
+  PushParams p{};
+  p.k_in = reinterpret_cast<const uint4*>(k);
+  p.v_in = reinterpret_cast<const uint4*>(v);
+  p.kv_k = reinterpret_cast<uint4*>(ctx->kv_k);
+  p.kv_v = reinterpret_cast<uint4*>(ctx->kv_v);
+  p.S = c.streams;
+  p.T = c.frames_T;
+  p.L = c.tokens_L;
+  p.HD = c.heads_H * c.head_dim;
+  p.M = c.sink_M;
+  p.R = c.ring_R;
+  p.head_dim = c.head_dim;
+  p.F = ctx->F;
+  p.p0 = (int32_t)p0;
+  p.rope_on = (int32_t)c.rope_on;
+  p.grid_w = (int32_t)(c.grid_w > 0 ? c.grid_w : 1);
+  for (int a = 0; a < 3; ++a) {
+    p.rope_seg[a] = ctx->rope_seg[a];
+    p.tab_off[a] = ctx->tab_off[a];
+  }
+  p.rope_tab = ctx->rope_tab;
+  cudaError_t e = launch_kv_push(p, ctx->sm_count, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "kv_push launch");
+  ctx->o = o;
+  ctx->p0 = p0;
+  if (reset) ctx->resets++;
+  ctx->chunk_first = ctx->F;
+  ctx->F += c.frames_T;
+  ctx->chunks++;
+  return SDS_OK;
+}
+
+sds_status sds_sink_refresh(sds_ctx* ctx, const float* chunk_emb, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (ctx->image_mode) return fail(ctx, SDS_ERR_STATE, "sink_refresh: context is in image batch mode");
+  const sds_config& c = ctx->cfg;
+  if (c.sink_M == 0) return SDS_OK;
+  if (ctx->chunk_first < 0) return fail(ctx, SDS_ERR_STATE, "sink_refresh before the first kv_push");
+  if (!chunk_emb || !aligned16(chunk_emb))
+    return fail(ctx, SDS_ERR_INVALID_ARG, "sink_refresh: chunk_emb must be a 16-byte aligned device pointer");
+  SinkParams p{};
+  p.h = chunk_emb;
+  p.emb = ctx->sink_emb;
+  p.kv_k = reinterpret_cast<uint4*>(ctx->kv_k);
+  p.kv_v = reinterpret_cast<uint4*>(ctx->kv_v);
+  p.state = ctx->state;
+  p.counters = ctx->counters + 1;
+  p.S = c.streams;
+  p.D = c.emb_dim_D;
+  p.M = c.sink_M;
+  p.R = c.ring_R;
+  p.L = c.tokens_L;
+  p.HD = c.heads_H * c.head_dim;
+  p.chunk_first = ctx->chunk_first;
+  p.s_th = c.s_th;
+  int64_t nfill = 0;
+  if (ctx->sinks_filled < c.sink_M) {
+    nfill = std::min<int64_t>(c.sink_M - ctx->sinks_filled, c.frames_T);
+    p.fill_from = ctx->sinks_filled;
+    p.fill_count = nfill;
+  } else {
+    p.fill_from = -1;
+    p.fill_count = 0;
+  }
+  cudaError_t e = launch_sink_refresh(p, ctx->sm_count, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "sink_refresh launch");
+  ctx->sinks_filled += nfill;
+  return SDS_OK;
+}
+
+static sds_status attend_common(sds_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, AttnParams& ap, int head_dim, int S,
+                                cudaStream_t st) {
+  cudaError_t e = launch_attention(tq, tk, tv, ap, head_dim, S, st);
+  if (e != cudaSuccess) {
+    if (ctx) return cuda_fail(ctx, e, "attention launch");
+    return fail(nullptr, SDS_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  }
+  return SDS_OK;
+}
+
+sds_status sds_attend(sds_ctx* ctx, const void* q, void* o, const void* ext_k, const void* ext_v,
+                      sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  const sds_config& c = ctx->cfg;
+  if (!q || !o || !aligned16(q) || !aligned16(o))
+    return fail(ctx, SDS_ERR_INVALID_ARG, "attend: q and o must be non-NULL 16-byte aligned device pointers");
+  const int64_t S = c.streams, HD = c.heads_H * c.head_dim;
+  AttnParams ap{};
+  ap.o = reinterpret_cast<uint16_t*>(o);
+  ap.H = (int32_t)c.heads_H;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  ap.state = ctx->state;
+  CUtensorMap tq, tk, tv;
+  if (ctx->image_mode) {
+    if (!ext_k || !ext_v || !aligned16(ext_k) || !aligned16(ext_v))
+      return fail(ctx, SDS_ERR_INVALID_ARG, "attend: image mode needs 16-byte aligned ext_k and ext_v");
+    const int64_t rows = c.slots_n * c.tokens_L;
+    ap.q_rows = rows;
+    ap.seg_start[0] = 0;
+    ap.seg_count[0] = (int32_t)rows;
+    ap.seg_start[1] = 0;
+    ap.seg_count[1] = 0;
+    if (!make_tmap_bf16(&tq, q, HD, rows, S) || !make_tmap_bf16(&tk, ext_k, HD, rows, S) ||
+        !make_tmap_bf16(&tv, ext_v, HD, rows, S))
+      return fail(ctx, SDS_ERR_CUDA, "attend: cuTensorMapEncodeTiled failed");
+    fill_attn_rope(ctx, ap);
+    ap.rope_on = 0;
+    return attend_common(ctx, tq, tk, tv, ap, (int)c.head_dim, (int)S, (cudaStream_t)stream);
+  }
+  if (ext_k || ext_v) return fail(ctx, SDS_ERR_INVALID_ARG, "attend: ext_k/ext_v must be NULL in video mode");
+  if (ctx->chunk_first < 0) return fail(ctx, SDS_ERR_STATE, "attend before the first kv_push");
+  const int64_t rows = c.slots_n * c.frames_T * c.tokens_L;
+  ap.q_rows = rows;
+  const int64_t valid = std::min<int64_t>(ctx->F, c.ring_R);
+  ap.seg_start[0] = 0;
+  ap.seg_count[0] = (int32_t)(ctx->sinks_filled * c.tokens_L);
+  ap.seg_start[1] = (int32_t)(c.sink_M * c.tokens_L);
+  ap.seg_count[1] = (int32_t)(valid * c.tokens_L);
+  if (ctx->sinks_filled == c.sink_M) {  // one contiguous range: sinks then ring
+    ap.seg_count[0] = (int32_t)((c.sink_M + valid) * c.tokens_L);
+    ap.seg_start[1] = 0;
+    ap.seg_count[1] = 0;
+  }
+  if (!make_tmap_bf16(&tq, q, HD, rows, S))
+    return fail(ctx, SDS_ERR_CUDA, "attend: cuTensorMapEncodeTiled failed");
+  fill_attn_rope(ctx, ap);
+  return attend_common(ctx, tq, ctx->tm_kv_k, ctx->tm_kv_v, ap, (int)c.head_dim, (int)S,
+                       (cudaStream_t)stream);
+}
+
+sds_status sds_attention(const void* q, const void* k, const void* v, void* o, int64_t S,
+                         int64_t Lq, int64_t Lk, int64_t H, int64_t head_dim, sds_stream_t stream) {
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(nullptr, SDS_ERR_INVALID_ARG, "attention: pointers must be non-NULL and 16-byte aligned");
+  if (S < 1 || S > 65535 || H < 1 || H > 65535 || Lq < 1 || Lk < 1 || Lk > (1ll << 30) ||
+      Lq > (1ll << 31) - 128)
+    return fail(nullptr, SDS_ERR_INVALID_ARG, "attention: sizes out of range");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(nullptr, SDS_ERR_INVALID_ARG, "attention: head_dim must be 64 or 128");
+  const int64_t HD = H * head_dim;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16(&tq, q, HD, Lq, S) || !make_tmap_bf16(&tk, k, HD, Lk, S) ||
+      !make_tmap_bf16(&tv, v, HD, Lk, S))
+    return fail(nullptr, SDS_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed");
+  AttnParams ap{};
+  ap.o = reinterpret_cast<uint16_t*>(o);
+  ap.q_rows = Lq;
+  ap.H = (int32_t)H;
+  ap.seg_start[0] = 0;
+  ap.seg_count[0] = (int32_t)Lk;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  ap.rope_on = 0;
+  ap.tokens_L = 1;
+  ap.grid_w = 1;
+  ap.chunk_tokens = 1;
+  ap.state = nullptr;
+  return attend_common(nullptr, tq, tk, tv, ap, (int)head_dim, (int)S, (cudaStream_t)stream);
+}
+
+static sds_status fill_step(sds_ctx* ctx, StepParams& p) {
+  const sds_config& c = ctx->cfg;
+  p.S = c.streams;
+  p.state = ctx->state;
+  p.partials = ctx->partials;
+  p.counter = ctx->counters;
+  p.nb_u = ctx->nb_u;
+  p.nb_s = ctx->nb_s;
+  p.nb_m = ctx->nb_m;
+  p.N_s = c.slot_elems;
+  p.E = c.ssf_elems;
+  p.eta = c.ssf_eta;
+  p.max_skip = c.max_skip_frame;
+  p.ssf_ref = ctx->ssf_ref;
+  p.T = c.frames_T;
+  p.N_f = c.frame_elems;
+  p.mot_k = c.mot_k;
+  p.sigma = c.mot_sigma;
+  p.lam = c.mot_lambda;
+  p.s_min = c.s_min;
+  p.s_max = c.s_max;
+  return SDS_OK;
+}
+
+sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (!io) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: io is NULL");
+  const sds_config& c = ctx->cfg;
+  const int n = (int)c.slots_n;
+  auto okp = [](const void* p) { return p && aligned16(p); };
+  for (int i = 0; i < n; ++i) {
+    if (!okp(io->x[i]) || !okp(io->x0[i]) || !okp(io->eps_c[i]) || !okp(io->x_next[i]))
+      return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: slot %d arrays must be non-NULL and 16-byte aligned", i);
+    if (i < n - 1 && !okp(io->z[i]))
+      return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: z[%d] must be non-NULL and 16-byte aligned", i);
+  }
+  if (!okp(io->out) || !okp(io->x0_new) || !okp(io->eps_new))
+    return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: out, x0_new, eps_new must be non-NULL and 16-byte aligned");
+  if (io->ssf_frame) {
+    if (!c.ssf_on) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: ssf_frame given but ssf_on == 0");
+    if (!okp(io->ssf_frame) || !io->ssf_u)
+      return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: ssf_frame must be 16-byte aligned and ssf_u non-NULL");
+  }
+  if (io->motion_chunk) {
+    if (!c.motion_on) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: motion_chunk given but motion_on == 0");
+    if (!okp(io->motion_chunk)) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: motion_chunk must be 16-byte aligned");
+  }
+  StepParams p{};
+  fill_step(ctx, p);
+  p.n = n;
+  for (int i = 0; i < n; ++i) {
+    p.x[i] = io->x[i];
+    p.x0[i] = io->x0[i];
+    p.eps_c[i] = io->eps_c[i];
+    p.z[i] = (i < n - 1) ? io->z[i] : nullptr;
+    p.x_next[i] = io->x_next[i];
+    const double a = ctx->abar_slot[i];
+    p.c_sa[i] = (float)std::sqrt(a);
+    p.c_inv_s1a[i] = (float)(1.0 / std::sqrt(1.0 - a));
+    p.c_s1a[i] = (float)std::sqrt(1.0 - a);
+    p.c_inv_sa[i] = (float)(1.0 / std::sqrt(a));
+  }
+  if (c.cfg_type == 1) {
+    p.c_gamma = (float)c.gamma;
+    p.c_dg = (float)(c.delta * (1.0 - c.gamma));
+  } else {
+    p.c_gamma = 1.0f;
+    p.c_dg = 0.0f;
+  }
+  p.out = io->out;
+  p.x0_new = io->x0_new;
+  p.eps_new = io->eps_new;
+  p.ssf_frame = io->ssf_frame;
+  p.ssf_u = io->ssf_u;
+  if (io->motion_chunk) {
+    const int64_t par = ctx->motion_calls & 1;
+    p.mot_chunk = io->motion_chunk;
+    p.mot_prev_in = ctx->mot_prev + par * c.streams * c.frame_elems;
+    p.mot_prev_out = ctx->mot_prev + (par ^ 1) * c.streams * c.frame_elems;
+  }
+  cudaError_t e = launch_step(p, ctx->sm_count, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "step_update launch");
+  if (io->motion_chunk) ctx->motion_calls++;
+  return SDS_OK;
+}
+
+sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (!ctx->cfg.ssf_on) return fail(ctx, SDS_ERR_INVALID_ARG, "ssf: ssf_on == 0 in the config");
+  if (!frame || !aligned16(frame) || !u)
+    return fail(ctx, SDS_ERR_INVALID_ARG, "ssf: frame must be 16-byte aligned and u non-NULL");
+  StepParams p{};
+  fill_step(ctx, p);
+  p.n = 0;
+  p.ssf_frame = frame;
+  p.ssf_u = u;
+  cudaError_t e = launch_step(p, ctx->sm_count, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "ssf launch");
+  return SDS_OK;
+}
+
+sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (!out) return fail(ctx, SDS_ERR_INVALID_ARG, "read_state: out is NULL");
+  const int64_t S = ctx->cfg.streams;
+  std::vector<DevState> tmp((size_t)S);
+  cudaError_t e = cudaMemcpyAsync(tmp.data(), ctx->state, (size_t)S * sizeof(DevState),
+                                  cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "read_state");
+  for (int64_t s = 0; s < S; ++s) out[s] = tmp[(size_t)s].pub;
+  return SDS_OK;
+}
+
+sds_status sds_get_meta(const sds_ctx* ctx, sds_meta* out) {
+  if (!ctx || !out) return fail(nullptr, SDS_ERR_INVALID_ARG, "get_meta: NULL argument");
+  out->frames_pushed = ctx->F;
+  out->rope_offset = ctx->o;
+  out->chunk_p0 = ctx->p0;
+  out->ring_valid = std::min<int64_t>(ctx->F, ctx->cfg.ring_R);
+  out->sinks_filled = ctx->sinks_filled;
+  out->rope_resets = ctx->resets;
+  out->chunks = ctx->chunks;
+  return SDS_OK;
+}
+
+sds_status sds_get_buffers(const sds_ctx* ctx, sds_buffers* out) {
+  if (!ctx || !out) return fail(nullptr, SDS_ERR_INVALID_ARG, "get_buffers: NULL argument");
+  out->kv_k = ctx->kv_k;
+  out->kv_v = ctx->kv_v;
+  out->sink_emb = ctx->sink_emb;
+  out->kv_rows = (ctx->cfg.sink_M + ctx->cfg.ring_R) * ctx->cfg.tokens_L;
+  return SDS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+// sds_internal.h -- declarations shared by the library's translation units
+// (host API in sds_api.cu, kernels in k_*.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/sds.h"
+
+namespace sds {
+
+constexpr int kMaxMotionWindow = 64;
+
+// Device-side per-stream record: the exported decisions plus private state.
+struct DevState {
+  sds_stream_state pub;
+  int64_t ssf_cur;     // which of the two reference buffers holds I_ref
+  int64_t mot_count;   // values in the window (<= mot_k)
+  int64_t mot_head;    // next write position in the circular window
+  int64_t mot_has_prev;
+  double mot_window[kMaxMotionWindow];
+};
+
+// Error bits recorded in DevState::pub.error_word.
+enum : int64_t {
+  kErrAttnWaitTimeout = 1 << 0,
+  kErrAttnBadShape = 1 << 1,
+  kErrStepBadArgs = 1 << 2,
+  kErrSinkBadArgs = 1 << 3,
+};
+
+// ----------------------------------------------------------------- K1 attention
+struct AttnParams {
+  uint16_t* o;           // bf16 [S][q_rows][H][d]
+  int64_t q_rows;        // query rows per stream
+  int32_t H;
+  int32_t seg_start[2];  // key row ranges inside the K/V tensor of a stream
+  int32_t seg_count[2];
+  float scale_log2;      // log2(e) / sqrt(d)
+  int32_t rope_on;
+  int32_t p0;            // temporal position of frame 0 of the chunk
+  int32_t tokens_L, grid_w, chunk_tokens;
+  int32_t rope_seg[3];   // d_t, d_y, d_x
+  const float2* rope_tab;
+  int32_t tab_off[3];    // entry offset of each axis table
+  DevState* state;       // per stream, for error reporting (may be null)
+};
+
+// q/k/v tensor maps: 3-D {H*d, rows, S}, box {64, 128, 1}, 128-byte swizzle.
+cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnParams& p, int head_dim, int S, cudaStream_t st);
+
+// Build a bf16 3-D tensor map {H*d, rows, S} with a {64, 128, 1} box.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t hd, int64_t rows, int64_t S);
+
+// ----------------------------------------------------------------- K2 / K3
+struct PushParams {
+  const uint4* k_in;  // bf16 [S][T*L][H*d] as 8-element vectors
+  const uint4* v_in;
+  uint4* kv_k;        // bf16 [S][(M+R)*L][H*d]
+  uint4* kv_v;
+  int64_t S, T, L, HD, M, R, head_dim;
+  int64_t F;          // frames pushed before this chunk
+  int32_t p0, rope_on, grid_w;
+  int32_t rope_seg[3];
+  const float2* rope_tab;
+  int32_t tab_off[3];
+};
+cudaError_t launch_kv_push(const PushParams& p, int sm_count, cudaStream_t st);
+
+struct SinkParams {
+  const float* h;       // [S][D]
+  float* emb;           // [S][M][D]
+  uint4* kv_k;          // bf16 [S][(M+R)*L][H*d]
+  uint4* kv_v;
+  DevState* state;
+  unsigned int* counters;  // [S], zero between launches
+  int64_t S, D, M, R, L, HD;
+  int64_t chunk_first;  // global index of frame 0 of the chunk just pushed
+  int64_t fill_from;    // >= 0: fill mode, first empty sink; < 0: similarity test
+  int64_t fill_count;
+  double s_th;
+};
+cudaError_t launch_sink_refresh(const SinkParams& p, int sm_count, cudaStream_t st);
+
+// ----------------------------------------------------------------- K4
+struct StepParams {
+  // update segment
+  const float* x[SDS_MAX_SLOTS];
+  const float* x0[SDS_MAX_SLOTS];
+  const float* eps_c[SDS_MAX_SLOTS];
+  const float* z[SDS_MAX_SLOTS];
+  float* x_next[SDS_MAX_SLOTS];
+  float* out;
+  const float* x0_new;
+  const float* eps_new;
+  float c_sa[SDS_MAX_SLOTS];       // sqrt(abar_i)
+  float c_inv_s1a[SDS_MAX_SLOTS];  // 1 / sqrt(1 - abar_i)
+  float c_s1a[SDS_MAX_SLOTS];      // sqrt(1 - abar_i)
+  float c_inv_sa[SDS_MAX_SLOTS];   // 1 / sqrt(abar_i)
+  float c_gamma, c_dg;             // gamma, delta * (1 - gamma)
+  int32_t n;                       // slots (0: no update segment)
+  int64_t N_s;
+  // SSF segment
+  const float* ssf_frame;          // null: no SSF
+  const float* ssf_u;
+  float* ssf_ref;                  // [2][S][E]
+  int64_t E;
+  double eta;
+  int64_t max_skip;
+  // motion segment
+  const float* mot_chunk;          // null: no motion; [S][T][N_f]
+  const float* mot_prev_in;        // [S][N_f]
+  float* mot_prev_out;             // [S][N_f]
+  int64_t T, N_f, mot_k;
+  double sigma, lam, s_min, s_max;
+  // common
+  int64_t S;
+  DevState* state;
+  double* partials;
+  unsigned int* counter;
+  int64_t nb_u, nb_s, nb_m;        // work blocks per stream (per pair for motion)
+};
+constexpr int kStepThreads = 256;
+constexpr int kStepBlockElems = 2048;  // elements per work block (8 per thread)
+cudaError_t launch_step(const StepParams& p, int sm_count, cudaStream_t st);
+
+}  // namespace sds

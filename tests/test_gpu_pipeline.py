@@ -1,0 +1,194 @@
+"""GPU parity of the whole per-step path (K2 push, K3 sink refresh, K1
+attend, K4 fused update + SSF + motion) against the oracle, over seeded
+multi-chunk sequences.
+
+Bars: ring indices, RoPE positions, sink choices and skip decisions
+bit-exact (a decision the oracle flags as a near tie may go either way);
+ring V bit-exact, ring K within max(1 bf16 ulp, 2^-20 * pair norm) (fp32 vs
+double rotation: near-zero results carry the fp32 error of the pair);
+attention within 2e-2 of the block max; the fp32 latent update within 1e-5
+of the tensor max; cosines within 1e-6; motion and noise rate within 1e-5.
+"""
+import numpy as np
+import pytest
+
+from streaming_diffusion_stream_b300 import workloads as W
+from tests.harness import (GpuPipe, OraclePipe, attn_rel_err, rope_k_excess, tensor_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-2
+UPD_TOL = 1e-5
+
+
+def sample_rows(nrows: int, k: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    edge = [0, 1, 127, 128, nrows // 2, nrows - 129, nrows - 128, nrows - 2, nrows - 1]
+    pick = rng.choice(nrows, size=min(k, nrows), replace=False)
+    rows = np.unique(np.clip(np.concatenate([edge, pick]), 0, nrows - 1))
+    return rows.astype(np.int64)
+
+
+def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_kv_every=1,
+                 ssf=None, motion=None):
+    """Run `steps` chunks through both paths and compare everything each step."""
+    ssf = w["ssf"] if ssf is None else ssf
+    motion = w["motion"] if motion is None else motion
+    S = w["streams"]
+    g, o = GpuPipe(w), OraclePipe(w)
+    emb, lat_walk, frames = W.EmbeddingWalk(w), W.LatentWalk(w), W.FrameWalk(w)
+    ssf_live = [True] * S
+    stats = dict(sink_fires=0, resets=0, skips=0, near=0)
+    try:
+        for step in range(steps):
+            k, v = W.gen_kv(w, step)
+            g.push(k, v)
+            o.push(k, v)
+            m, om = g.meta(), o.s[0].meta()
+            assert (m["frames_pushed"], m["rope_offset"], m["chunk_p0"], m["ring_valid"]) == \
+                (om["F"], om["o"], om["p0"], om["valid"]), step
+            h = emb.next()
+            g.refresh(h)
+            ores = o.refresh(h)
+            st = g.state()
+            assert g.meta()["sinks_filled"] == o.s[0].meta()["sinks_filled"]
+            for s in range(S):
+                r = ores[s]
+                if r["near"]:
+                    stats["near"] += 1
+                    continue
+                if r["fire"] == 0 and r["j"] < 0:
+                    continue
+                assert st[s]["sink_fire"] == r["fire"], (step, s, st[s], r)
+                assert st[s]["sink_j"] == r["j"], (step, s)
+                if r["fire"] == 1:
+                    stats["sink_fires"] += 1
+                if r["fire"] != 2:
+                    assert abs(st[s]["sink_alpha_min"] - r["alpha_min"]) < 1e-12
+            if step % check_kv_every == 0 or step == steps - 1:
+                gk, gv = g.kv()
+                for s in range(S):
+                    ok, ov = o.s[s].kv()
+                    assert np.array_equal(gv[s], ov), (step, s)
+                    assert rope_k_excess(gk[s], ok) <= 1.0, (step, s)
+                if w["M"] > 0:
+                    ge = g.sink_emb()
+                    for s in range(S):
+                        filled = o.s[s].meta()["sinks_filled"]
+                        assert np.array_equal(ge[s][:filled].astype(np.float64), o.s[s].emb()[:filled])
+            if step % attend_every == 0 or step == steps - 1:
+                q = W.gen_q(w, step)
+                got = g.attend(q)
+                rows = None if rows_per_step is None else sample_rows(w["q_rows"], rows_per_step, step)
+                refs = o.attend(q, rows)
+                for s in range(S):
+                    gs = got[s] if rows is None else got[s][rows]
+                    err = attn_rel_err(gs, refs[s])
+                    assert err <= ATTN_TOL, (step, s, err)
+            lat = W.gen_latents(w, step)
+            frame = frames.next() if ssf else None
+            u = W.gen_u(w, step) if ssf else None
+            chunk = lat_walk.next() if motion else None
+            xn, out = g.step(lat, frame, u, chunk)
+            ores = o.step(lat)
+            for s in range(S):
+                xr, outr = ores[s]
+                assert tensor_rel_err(out[s], outr) <= UPD_TOL, (step, s)
+                for i in range(w["n"]):
+                    assert tensor_rel_err(xn[i, s], xr[i]) <= UPD_TOL, (step, s, i)
+            st = g.state()
+            if ssf:
+                oss = o.ssf(frame, u)
+                for s in range(S):
+                    if not ssf_live[s]:
+                        continue
+                    assert abs(st[s]["ssf_cos"] - oss[s]["cos"]) <= 1e-6, (step, s)
+                    assert abs(st[s]["ssf_p"] - oss[s]["p"]) <= 5e-5, (step, s)
+                    if oss[s]["near"] and st[s]["ssf_skip"] != oss[s]["skip"]:
+                        ssf_live[s] = False  # a flagged near tie went the other way
+                        stats["near"] += 1
+                        continue
+                    assert st[s]["ssf_skip"] == oss[s]["skip"], (step, s, st[s], oss[s])
+                    assert st[s]["ssf_skip_count"] == oss[s]["skip_count"]
+                    stats["skips"] += oss[s]["skip"]
+            if motion:
+                om_ = o.motion(chunk)
+                for s in range(S):
+                    dref = om_[s]["d"]
+                    dg = np.array(st[s]["motion_d"][:w["T"]])
+                    assert np.array_equal(np.isnan(dg), np.isnan(dref)), (step, s)
+                    ok_ = ~np.isnan(dref)
+                    assert np.all(np.abs(dg[ok_] - dref[ok_]) <= 1e-5 * np.maximum(1.0, dref[ok_]))
+                    assert abs(st[s]["noise_rate"] - om_[s]["s"]) <= 1e-5, (step, s)
+            for s in range(S):
+                assert st[s]["error_word"] == 0
+        stats["resets"] = o.s[0].meta()["resets"]
+        assert g.meta()["rope_resets"] == stats["resets"]
+        return stats
+    finally:
+        g.close()
+
+
+def test_c1_tiny_sequence_all_rows():
+    w = W.get_config("c1_tiny")
+    stats = run_sequence(w, w["steps"])
+    assert stats["sink_fires"] >= 1  # the embedding walk of c1 crosses s_th within 8 chunks
+
+
+def test_c1_two_streams():
+    w = W.get_config("c1_tiny", streams=2, steps=6)
+    run_sequence(w, 6)
+
+
+def test_rope_reset_fires_with_small_tau():
+    w = W.get_config("c1_tiny", rope_tau=3, steps=11)
+    stats = run_sequence(w, 11)
+    assert stats["resets"] == 2  # p0: 0 1 2 3 | 0 1 2 3 | 0 1 2
+
+
+def test_multi_sink_fill_and_refresh_with_chunks_of_three():
+    w = W.get_config("c1_tiny", M=2, T=3, R=6, mot_k=3, emb_step=0.5, latent_h=4, latent_w=4)
+    run_sequence(w, 7)
+
+
+def test_c3_full_size_sampled_rows():
+    w = W.get_config("c3_dit1p3b_video")
+    run_sequence(w, 4, rows_per_step=40, attend_every=3)
+
+
+def test_c4_full_size_sampled_rows():
+    w = W.get_config("c4_dit14b_video")
+    run_sequence(w, 5, rows_per_step=16, attend_every=4, check_kv_every=4)
+
+
+def test_c2_image_stream_update_and_ssf():
+    """Image batch mode at full size: fused update + SSF over 12 frames."""
+    w = W.get_config("c2_sdturbo_image")
+    g, o = GpuPipe(w), OraclePipe(w)
+    frames = W.FrameWalk(w)
+    try:
+        for step in range(12):
+            lat = W.gen_latents(w, step)
+            frame, u = frames.next(), W.gen_u(w, step)
+            xn, out = g.step(lat, frame, u)
+            (xr, outr), = o.step(lat)
+            assert tensor_rel_err(out[0], outr) <= UPD_TOL
+            for i in range(w["n"]):
+                assert tensor_rel_err(xn[i, 0], xr[i]) <= UPD_TOL
+            st = g.state()[0]
+            ref = o.ssf(frame, u)[0]
+            assert abs(st["ssf_cos"] - ref["cos"]) <= 1e-6
+            if not ref["near"]:
+                assert st["ssf_skip"] == ref["skip"] and st["ssf_skip_count"] == ref["skip_count"]
+            else:
+                break
+    finally:
+        g.close()
+
+
+def test_c5_stress_three_streams_with_bursts():
+    """Long-run shape with 3 concurrent streams: refreshes and bursts; K/V
+    compared every 10 chunks, attention sampled at the end."""
+    w = W.get_config("c5_stress", streams=3, burst_prob=0.2, emb_step=0.4)
+    stats = run_sequence(w, 30, rows_per_step=12, attend_every=29, check_kv_every=10)
+    assert stats["sink_fires"] >= 1
