@@ -53,11 +53,15 @@ def parse():
     return ap.parse_args()
 
 
-def workload(args) -> dict:
+def workload(args, rank: int = 0) -> dict:
+    """The workload one rank serves.  Ranks are independent replicas serving
+    their own streams, so each rank draws its inputs from its own seed."""
     over = {}
     if args.streams:
         over["streams"] = args.streams
-    return W.get_config(args.workload, **over)
+    w = W.get_config(args.workload, **over)
+    w["seed"] = w["seed"] + 1000 * rank
+    return w
 
 
 def frames_per_step(w: dict) -> int:
@@ -302,19 +306,26 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's value (timing only: the data path has no collective)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(frames_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job frames/s: all ranks' frames over the slowest rank's time."""
+    return frames_per_rank * world / (ms_max / 1e3)
 
 
 def run_ours(args):
     import torch
     rank, world = dist_setup(args.gpus)
-    w = workload(args)
+    w = workload(args, rank)
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     run = Runner(w, pool_bytes_min=2.0 * l2)
@@ -354,8 +365,7 @@ def run_ours(args):
     per_kernel = {n: float(np.mean([ev[n][0][i].elapsed_time(ev[n][1][i]) for i in range(steps)]))
                   for n in names}
     ms_step = ms_total / steps
-    frames = frames_per_step(w) * steps * world
-    value = frames / (ms_total / 1e3)
+    value = aggregate(frames_per_step(w) * steps, ms_total, world)
 
     # ---- end to end through the public API with host buffers
     e2e = None
