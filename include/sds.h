@@ -307,6 +307,42 @@ SDS_API sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stre
  */
 SDS_API sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds_stream_t stream);
 
+/*
+ * Allocation-free similarity filter.  The pages have no counterpart: it is
+ * a service of this library for callers that cannot allocate device memory
+ * -- code working inside a fixed device-memory budget owned by another
+ * allocator, or in a latency-critical loop where cudaMalloc/cudaFree (which
+ * may synchronise the device) are not allowed -- and so cannot create a
+ * context.  It computes what sds_ssf computes, on a reference frame the
+ * caller supplies instead of the context's stored one, with the same
+ * arithmetic (same cosine, probability and decision for the same inputs),
+ * and it calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   frame, ref  device fp32 [S][E]: incoming frame and reference frame
+ *   u           device fp32 [S]: uniform draws in [0,1)
+ *   skip_count  device int64 [S] consecutive skips so far, or NULL (all 0)
+ *   cos_out, p_out  device double [S]; skip_out device int64 [S]
+ *   skip = (u < P) and (skip_count < max_skip)
+ *
+ * Scratch: a static device array of SDS_NOALLOC_SCRATCH_BYTES (256 KiB) in
+ * the library, present on every GPU that loads the library until the process
+ * exits.  Its reduction partials limit the size: S * ceil(E / 2048) * 3 must
+ * not exceed SDS_NOALLOC_MAX_PARTIALS (32736; e.g. S <= 28 streams of
+ * 3x512x512 frames); larger requests fail with SDS_ERR_INVALID_ARG and a
+ * message in sds_last_error(NULL).  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call
+ * shares the one array and clears its counter on `stream` before use, so
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it: order them.
+ */
+#define SDS_NOALLOC_SCRATCH_BYTES 262144
+#define SDS_NOALLOC_MAX_PARTIALS 32736
+SDS_API sds_status sds_ssf_noalloc(const float* frame, const float* ref, const float* u,
+                                   const int64_t* skip_count, int64_t S, int64_t E, double eta,
+                                   int64_t max_skip, double* cos_out, double* p_out,
+                                   int64_t* skip_out, sds_stream_t stream);
+
 /* Synchronise `stream` and copy the S per-stream decision records to host
  * memory out[0..S-1]. */
 SDS_API sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream);

@@ -79,6 +79,7 @@ SIGNATURES = {
     "sds_attention": (C.c_int, [_P, _P, _P, _P, _i64, _i64, _i64, _i64, _i64, _P]),
     "sds_step_update": (C.c_int, [_P, C.POINTER(sds_step_io), _P]),
     "sds_ssf": (C.c_int, [_P, _P, _P, _P]),
+    "sds_ssf_noalloc": (C.c_int, [_P, _P, _P, _P, _i64, _i64, _f64, _i64, _P, _P, _P, _P]),
     "sds_read_state": (C.c_int, [_P, C.POINTER(sds_stream_state), _P]),
     "sds_get_meta": (C.c_int, [_P, C.POINTER(sds_meta)]),
     "sds_get_buffers": (C.c_int, [_P, C.POINTER(sds_buffers)]),
@@ -218,6 +219,15 @@ def sds_step_update(ctx, io: sds_step_io, stream=None):
 
 def sds_ssf(ctx, frame, u, stream=None):
     check(lib().sds_ssf(ctx, _ptr(frame), _ptr(u), _stream(stream)), ctx)
+
+
+def sds_ssf_noalloc(frame, ref, u, skip_count, S, E, eta, max_skip, cos_out, p_out, skip_out,
+                    stream=None):
+    """Allocation-free similarity filter (see include/sds.h): all arguments are
+    caller-owned device tensors; the library allocates nothing."""
+    check(lib().sds_ssf_noalloc(_ptr(frame), _ptr(ref), _ptr(u), _ptr(skip_count), S, E, eta,
+                                max_skip, _ptr(cos_out), _ptr(p_out), _ptr(skip_out),
+                                _stream(stream)))
 
 
 def sds_read_state(ctx, streams: int, stream=None) -> list[dict]:

@@ -171,6 +171,8 @@ void fill_attn_rope(const sds_ctx* c, AttnParams& ap) {
 
 }  // namespace
 
+void sds::set_thread_error(const char* msg) { g_create_err = msg; }
+
 extern "C" {
 
 int sds_abi_version(void) { return SDS_ABI_VERSION; }

@@ -123,6 +123,9 @@ struct StepParams {
   unsigned int* counter;
   int64_t nb_u, nb_s, nb_m;        // work blocks per stream (per pair for motion)
 };
+// Message for sds_last_error(NULL) from entry points without a context.
+void set_thread_error(const char* msg);
+
 constexpr int kStepThreads = 256;
 constexpr int kStepBlockElems = 2048;  // elements per work block (8 per thread)
 cudaError_t launch_step(const StepParams& p, int sm_count, cudaStream_t st);
