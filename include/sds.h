@@ -61,7 +61,7 @@ extern "C" {
 #define SDS_API
 #endif
 
-#define SDS_ABI_VERSION 1
+#define SDS_ABI_VERSION 2
 #define SDS_MAX_SLOTS 8
 #define SDS_MAX_CHUNK_FRAMES 8
 
@@ -111,6 +111,12 @@ typedef enum {
  *
  * mem_cap_bytes: if nonzero, sds_create fails with SDS_ERR_OOM when the
  * context's device memory would exceed it (no allocation is attempted).
+ *
+ * attn_ctas: 0 lets sds_attend choose its grid (one CTA per pair of 128-row
+ * query tiles, or, when that leaves a ragged last wave on a large problem,
+ * one persistent CTA per SM with the keys of some tiles split between CTAs).
+ * A positive value forces the persistent split schedule on at most that
+ * many CTAs (capped at 160), e.g. to leave SMs to concurrent work.
  */
 typedef struct {
   int64_t abi_version; /* must equal SDS_ABI_VERSION */
@@ -123,6 +129,7 @@ typedef struct {
   int64_t ssf_on, ssf_elems, max_skip_frame;
   int64_t motion_on, frame_elems, mot_k;
   int64_t mem_cap_bytes;
+  int64_t attn_ctas;
   double rope_base, s_th, beta_start, beta_end, gamma, delta, ssf_eta;
   double mot_sigma, mot_lambda, s_min, s_max;
 } sds_config;

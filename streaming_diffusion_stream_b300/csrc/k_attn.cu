@@ -6,28 +6,47 @@
 // In video mode the key set is the sink + rolling ring of cached frames
 // (StreamDiffusionV2 summary, sink tokens + rolling KV cache).
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (stream, head); both
-// share every 128-key K/V tile.  Warp roles:
+// Work decomposition.  A work item is a pair of 128-row query tiles (Q0, Q1)
+// of one (stream, head) against all of its keys, processed as 128-key
+// tiles.  The (item, key tile) units of a launch are divided evenly over a
+// persistent grid (one CTA per SM), so a CTA may start or stop inside an
+// item.  A CTA that covers only part of an item's keys writes its partial
+// result (unnormalised O, running max m, running sum l per row) to a
+// workspace and counts itself in per-row arrival counters; the contributor
+// that arrives last merges the partials and writes the output.  Nobody
+// waits for anybody, so a slow CTA cannot stall another.  Without a
+// workspace the grid has one CTA per item and nothing is split.
+//
+// Warp roles inside a CTA:
 //   warps 0-3  softmax group 0 (tile Q0), one query row per thread = one TMEM lane
 //   warps 4-7  softmax group 1 (tile Q1)
-//   warp  8    TMA producer: Q once, then K and V tiles through an ST-stage ring
+//   warp  8    TMA producer: K and V tiles through an ST-stage ring, Q per item
 //   warp  9    MMA issuer (one thread): tcgen05.mma into tensor memory
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256) fp32 scores;
 // O0 [256, 256+d), O1 [384, 384+d) fp32 accumulators.  Each group writes its
 // probabilities P as packed bf16 over the first 64 columns of its own S
 // region, and O += P V reads P straight from tensor memory (A operand in
 // TMEM), so P never touches shared memory.  The MMA issuer interleaves
-//   PV0(j), S0(j+1), PV1(j), S1(j+1), ...
+//   PV0(g), S0(g+1), PV1(g), S1(g+1), ...
 // so the tensor core works on one group's tile while the other group runs
-// its softmax (ping-pong).  tcgen05 MMAs run in issue order, so S0(j+1) may
-// overwrite the P0(j) columns that PV0(j) reads.
+// its softmax (ping-pong); the waits for K/V data, which the producer lands
+// several tiles ahead, are taken before the wait for P so they stay off the
+// critical path.  tcgen05 MMAs run in issue order, so S_t(g+1) may
+// overwrite the P_t(g) columns that PV_t(g) reads.
 // The online softmax keeps a running max m per row and rescales O (in
 // tensor memory) only when a tile raises m by more than 8 (log2 units):
 // otherwise probabilities may exceed 1 by up to 2^8, which fp32 sums and bf16
-// P hold without loss.  Every wait has a time limit; on expiry the kernel
-// records kErrAttnWaitTimeout in the stream's error word and leaves.
+// P hold without loss.  So after an item's first tile the exponentials are
+// taken against the running max straight away, with the tile max computed
+// alongside on another pipe; the rare tile that raises the max past the
+// threshold is redone against its own max.  Score scaling and row sums use packed f32x2
+// arithmetic and the row max a three-input max, halving their instruction
+// count.  Every wait has a time limit; on expiry the kernel records
+// kErrAttnWaitTimeout in the error word of every stream and leaves.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -36,19 +55,24 @@
 namespace sds {
 namespace {
 
-constexpr int BM = 128;         // query rows per tile (two tiles per CTA)
+constexpr int BM = 128;         // query rows per tile (two tiles per item)
 constexpr int BN = 128;         // keys per tile
 constexpr int SUB = 128 * 128;  // bytes of one 128-row x 64-column bf16 sub-tile
-constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA
+constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA issuer
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
 struct Cfg {
   static constexpr int NSUB = D / 64;
   static constexpr int TILE = NSUB * SUB;  // one 128-row tile of Q, K or V
-  static constexpr int ST = (D == 64) ? 4 : 2;
+  static constexpr int ST = (D == 64) ? 4 : 2;  // K/V pipeline stages
+  static constexpr int QB = (D == 64) ? 2 : 1;  // Q buffers (double-buffered across items if it fits)
+  // d = 64 leaves 64 spare tensor-memory columns after each O accumulator:
+  // P goes there, S stays intact, and exponentials are taken speculatively
+  // against the running max (a tile that raises it is redone from S).
+  static constexpr bool SPEC = (D == 64);
   static constexpr int Q = 0;
-  static constexpr int K = Q + 2 * TILE;
+  static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
   static constexpr int BAR = V + ST * TILE;
   static constexpr int TOTAL = BAR + 512;
@@ -60,9 +84,16 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 struct Bars {
-  uint64_t* q_full;
-  uint64_t* q_ready;
+  uint64_t* q_full;   // [2]
+  uint64_t* q_ready;  // [2][2]: buffer, tile
+  uint64_t* q_empty;  // [2]
   uint64_t* k_full;
   uint64_t* v_full;
   uint64_t* k_empty;
@@ -81,8 +112,9 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   uint64_t* b = reinterpret_cast<uint64_t*>(sm + C::BAR);
   Bars r;
   r.q_full = b;
-  r.q_ready = b + 1;
-  r.k_full = b + 2;
+  r.q_ready = b + 2;
+  r.q_empty = b + 6;
+  r.k_full = b + 8;
   r.v_full = r.k_full + C::ST;
   r.k_empty = r.v_full + C::ST;
   r.v_empty = r.k_empty + C::ST;
@@ -107,6 +139,60 @@ __device__ __forceinline__ void key_tile(const AttnParams& p, int nt0, int j, in
 
 __device__ __forceinline__ void fail_wait(const Bars& B) { *B.abort_flag = 1; }
 
+// The even division of U units over G CTAs: CTA c owns [lo(c), lo(c+1)).
+struct Split {
+  int64_t U, G, nkt;
+  __device__ __forceinline__ int64_t lo(int64_t c) const { return c * U / G; }
+  // the CTA whose range holds unit u
+  __device__ __forceinline__ int64_t owner(int64_t u) const { return ((u + 1) * G - 1) / U; }
+};
+
+// Walk over one CTA's units: global tile counter g, segment counter sg
+// (one segment per item touched), the item and its key-tile range.
+struct SegIter {
+  int64_t u, u_hi, seg_lo, seg_hi, item, nkt;
+  int64_t g;
+  int sg;
+  __device__ __forceinline__ void init(int64_t lo, int64_t hi, int64_t nkt_) {
+    u = lo;
+    u_hi = hi;
+    nkt = nkt_;
+    g = 0;
+    sg = 0;
+    start_segment();
+  }
+  __device__ __forceinline__ void start_segment() {
+    item = u / nkt;
+    seg_lo = u;
+    seg_hi = min(u_hi, (item + 1) * nkt);
+  }
+  __device__ __forceinline__ bool done() const { return u >= u_hi; }
+  __device__ __forceinline__ bool first() const { return u == seg_lo; }
+  __device__ __forceinline__ bool last() const { return u + 1 == seg_hi; }
+  __device__ __forceinline__ int kt() const { return (int)(u - item * nkt); }
+  __device__ __forceinline__ void advance() {
+    ++u;
+    ++g;
+    if (u == seg_hi && u < u_hi) {
+      ++sg;
+      start_segment();
+    }
+  }
+};
+
+struct ItemPos {
+  int s, h;
+  int64_t q0;
+};
+__device__ __forceinline__ ItemPos item_pos(const AttnParams& p, int64_t item, int64_t npairs) {
+  ItemPos r;
+  const int64_t pair = item % npairs, sh = item / npairs;
+  r.h = (int)(sh % p.H);
+  r.s = (int)(sh / p.H);
+  r.q0 = pair * (2 * BM);
+  return r;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -121,17 +207,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = sm + C::V;
 
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, s = blockIdx.z;
-  const int q0 = blockIdx.x * (2 * BM);
   const int nt0 = (p.seg_count[0] + BN - 1) / BN;
-  const int nt = nt0 + (p.seg_count[1] + BN - 1) / BN;
+  const int64_t nkt = nt0 + (p.seg_count[1] + BN - 1) / BN;
+  const int64_t npairs = (p.q_rows + 2 * BM - 1) / (2 * BM);
+  Split sp;
+  sp.nkt = nkt;
+  sp.U = (int64_t)p.S * p.H * npairs * nkt;
+  sp.G = gridDim.x;
+  const int64_t cta = blockIdx.x;
+  const int64_t u_lo = sp.lo(cta), u_hi = sp.lo(cta + 1);
+  const bool active = nkt > 0 && u_hi > u_lo;
 
   if (tid == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
-    mbar_init(B.q_full, 1);
-    mbar_init(B.q_ready, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B.q_full + i, 1);
+      mbar_init(B.q_empty + i, 1);
+      mbar_init(B.q_ready + 2 * i + 0, 128);
+      mbar_init(B.q_ready + 2 * i + 1, 128);
+    }
     for (int i = 0; i < C::ST; ++i) {
       mbar_init(B.k_full + i, 1);
       mbar_init(B.v_full + i, 1);
@@ -158,195 +254,378 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (wid == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nt > 0) {
-      mbar_arrive_expect_tx(B.q_full, 2 * C::TILE);
-      for (int t = 0; t < 2; ++t)
-        for (int b = 0; b < C::NSUB; ++b)
-          tma_load_3d(sQ + t * C::TILE + b * SUB, &tm_q, h * D + b * 64, q0 + t * BM, s, B.q_full);
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int st = j % C::ST;
-        const uint32_t ph = (uint32_t)(j / C::ST) & 1u;
+    if (lane == 0 && active) {
+      SegIter it;
+      it.init(u_lo, u_hi, nkt);
+      int64_t issued_k = 0, issued_v = 0;  // tiles whose K / V copy was issued
+      int issued_q = 0;                    // segments whose Q copy was issued
+      bool ok = true;
+      while (ok && !it.done()) {
+        const int64_t g = it.g;
+        const int st = (int)(g % C::ST);
+        const uint32_t ph = (uint32_t)(g / C::ST) & 1u;
+        const ItemPos ip = item_pos(p, it.item, npairs);
         int key0, nvalid;
-        key_tile(p, nt0, j, key0, nvalid);
-        if (!mbar_wait(B.k_empty + st, ph ^ 1u)) { fail_wait(B); break; }
+        key_tile(p, nt0, it.kt(), key0, nvalid);
+        if (!mbar_wait(B.k_empty + st, ph ^ 1u)) { ok = false; break; }
         mbar_arrive_expect_tx(B.k_full + st, C::TILE);
         for (int b = 0; b < C::NSUB; ++b)
-          tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, h * D + b * 64, key0, s, B.k_full + st);
-        if (!mbar_wait(B.v_empty + st, ph ^ 1u)) {
-          issued = j;  // K of tile j is in flight; wait for it below
-          mbar_wait(B.k_full + st, ph);
-          fail_wait(B);
-          break;
-        }
+          tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, ip.h * D + b * 64, key0, ip.s, B.k_full + st);
+        issued_k = g + 1;
+        if (!mbar_wait(B.v_empty + st, ph ^ 1u)) { ok = false; break; }
         mbar_arrive_expect_tx(B.v_full + st, C::TILE);
         for (int b = 0; b < C::NSUB; ++b)
-          tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, h * D + b * 64, key0, s, B.v_full + st);
-        issued = j + 1;
+          tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
+        issued_v = g + 1;
+        if (it.first()) {
+          // this item's queries; the buffer is free once the last S MMAs
+          // of the item that used it before have completed
+          const int qb = it.sg % C::QB;
+          if (it.sg >= C::QB && !mbar_wait(B.q_empty + qb, (uint32_t)(it.sg / C::QB - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B.q_full + qb, 2 * C::TILE);
+          for (int t = 0; t < 2; ++t)
+            for (int b = 0; b < C::NSUB; ++b)
+              tma_load_3d(sQ + (qb * 2 + t) * C::TILE + b * SUB, &tm_q, ip.h * D + b * 64,
+                          (int32_t)(ip.q0 + t * BM), ip.s, B.q_full + qb);
+          issued_q = it.sg + 1;
+        }
+        it.advance();
       }
-      // leave only after every copy of ours has landed in shared memory
-      mbar_wait(B.q_full, 0);
-      for (int j = (issued > C::ST ? issued - C::ST : 0); j < issued; ++j) {
+      if (!ok) fail_wait(B);
+      // leave only after every copy we issued has landed in shared memory
+      for (int sgi = (issued_q > C::QB ? issued_q - C::QB : 0); sgi < issued_q; ++sgi)
+        mbar_wait(B.q_full + sgi % C::QB, (uint32_t)(sgi / C::QB) & 1u);
+      for (int64_t j = (issued_k > C::ST ? issued_k - C::ST : 0); j < issued_k; ++j)
         mbar_wait(B.k_full + j % C::ST, (uint32_t)(j / C::ST) & 1u);
+      for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
         mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u);
-      }
     }
   } else if (wid == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && active) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      auto issue_s = [&](int t, int st) {
+      // Descriptor words: the high word (stride 1024 B, fixed 0b001, 128-byte
+      // swizzle) is common to every operand; the low word holds the start
+      // address >> 4 and the leading-dimension offset, so stepping through a
+      // tile is a 32-bit add.
+      const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
+      const uint32_t qlo = (uint32_t)smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t klo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
+      auto issue_s = [&](int t, int qb, uint32_t st) {
         const uint32_t dS = tmem + (uint32_t)(t * 128);
+        const uint32_t a0 = qlo + (uint32_t)(((qb * 2 + t) * C::TILE) >> 4);
+        const uint32_t b0 = klo + st * (uint32_t)(C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * SUB + (kk & 3) * 32);
-          mma_bf16_ss(dS, smem_desc_sw128(aQ + t * C::TILE + off, 16, 1024),
-                      smem_desc_sw128(aK + st * C::TILE + off, 16, 1024), IDESC_S,
-                      kk > 0 ? 1u : 0u);
+          const uint32_t off = (uint32_t)(((kk >> 2) * SUB + (kk & 3) * 32) >> 4);
+          mma_bf16_ss_w(dS, a0 + off, dhi, b0 + off, dhi, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int st, bool acc) {
+      auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t dO = tmem + 256u + (uint32_t)(t * 128);
-        const uint32_t aP = tmem + (uint32_t)(t * 128);
+        const uint32_t aP = C::SPEC ? dO + 64u : tmem + (uint32_t)(t * 128);
+        const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_bf16_ts(dO, aP + (uint32_t)(kk * 8),
-                      smem_desc_sw128(aV + st * C::TILE + kk * 16 * 128, SUB, 1024), IDESC_O,
-                      (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4), dhi,
+                        IDESC_O, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(B.q_ready, 0) && mbar_wait(B.k_full, 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        mma_commit(B.s_full + 0);
-        issue_s(1, 0);
-        mma_commit(B.s_full + 1);
-        mma_commit(B.k_empty + 0);
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        const int st = j % C::ST;
-        const uint32_t ph = (uint32_t)(j / C::ST) & 1u;
-        const int st1 = (j + 1) % C::ST;
-        const uint32_t ph1 = (uint32_t)((j + 1) / C::ST) & 1u;
-        if (!mbar_wait(B.v_full + st, ph) || !mbar_wait(B.p_full + 0, (uint32_t)j & 1u)) {
-          ok = false;
-          break;
+      bool ok = true;
+      uint32_t g = 0;  // global tile counter
+      int sg = 0;      // segment counter
+      int64_t u = u_lo;
+      // segment 0: S of its first tile for both groups
+      {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        ok = mbar_wait(B.q_ready + 0, 0) && mbar_wait(B.k_full, 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          mma_commit(B.s_full + 0);
+          ok = mbar_wait(B.q_ready + 1, 0);
         }
-        tc_fence_after();
-        issue_pv(0, st, j > 0);
-        mma_commit(B.o_done + 0);
-        if (j + 1 < nt) {
-          if (!mbar_wait(B.k_full + st1, ph1)) {
+        if (ok) {
+          tc_fence_after();
+          issue_s(1, 0, 0);
+          mma_commit(B.s_full + 1);
+          mma_commit(B.k_empty + 0);
+          if (seg_hi - u == 1) mma_commit(B.q_empty + 0);
+        }
+      }
+      while (ok && u < u_hi) {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        const int n_here = (int)(seg_hi - u);
+        const bool final_seg = seg_hi == u_hi;
+        const int n_next = final_seg ? 0 : (int)(min(u_hi, seg_hi + nkt) - seg_hi);
+        const int qb_n = (sg + 1) % C::QB;
+        const uint32_t qp_n = (uint32_t)((sg + 1) / C::QB) & 1u;
+        for (int i = 0; i < n_here; ++i, ++g) {
+          const uint32_t st = g % C::ST, ph = (g / C::ST) & 1u;
+          const uint32_t st1 = (g + 1) % C::ST, ph1 = ((g + 1) / C::ST) & 1u;
+          const bool acc = i > 0;
+          const bool boundary = i + 1 == n_here;  // tile g+1 opens the next segment
+          const bool more = !(boundary && final_seg);
+          // tile g+1 is the last of its segment: its S MMAs release the Q buffer
+          const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
+          // the producer lands K/V tiles well ahead: wait for them first
+          if (!mbar_wait(B.v_full + st, ph) || (more && !mbar_wait(B.k_full + st1, ph1))) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(B.p_full + 0, g & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(0, st1);
-          mma_commit(B.s_full + 0);
+          issue_pv(0, st, acc);
+          mma_commit(B.o_done + 0);
+          const int qb1 = boundary ? qb_n : sg % C::QB;
+          if (more) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, qb1, st1);
+            mma_commit(B.s_full + 0);
+          }
+          if (!mbar_wait(B.p_full + 1, g & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(1, st, acc);
+          mma_commit(B.o_done + 1);
+          mma_commit(B.v_empty + st);
+          if (more) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(1, qb1, st1);
+            mma_commit(B.s_full + 1);
+            mma_commit(B.k_empty + st1);
+            if (next_last) mma_commit(B.q_empty + qb1);
+          }
         }
-        if (!mbar_wait(B.p_full + 1, (uint32_t)j & 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(1, st, j > 0);
-        mma_commit(B.o_done + 1);
-        mma_commit(B.v_empty + st);
-        if (j + 1 < nt) {
-          issue_s(1, st1);
-          mma_commit(B.s_full + 1);
-          mma_commit(B.k_empty + st1);
-        }
+        u = seg_hi;
+        ++sg;
       }
       if (!ok) fail_wait(B);
       // all our MMAs complete before tensor memory is released
       mma_commit(B.mma_final);
       mbar_wait(B.mma_final, 0);
     }
-  } else {
+  } else if (active) {
     // ------------------------------------------------------------ softmax groups
     const int t = wid >> 2;   // query tile of this group
     const int r = tid & 127;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((wid & 3) * 32) << 16;
     const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_base;
     const uint32_t tO = tmem + 256u + (uint32_t)(t * 128) + lane_base;
-    const int64_t row = (int64_t)q0 + t * BM + r;
-    bool ok = nt > 0 && mbar_wait(B.q_full, 0);
-    if (ok && p.rope_on && row < p.q_rows) {
-      const int tok = (int)(row % p.chunk_tokens);
-      const int jf = tok / p.tokens_L, l = tok % p.tokens_L;
-      const int pos[3] = {p.p0 + jf, l / p.grid_w, l % p.grid_w};
-      const int seg[3] = {p.rope_seg[0], p.rope_seg[1], p.rope_seg[2]};
-      const int off[3] = {p.tab_off[0], p.tab_off[1], p.tab_off[2]};
-#pragma unroll
-      for (int b = 0; b < C::NSUB; ++b) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4* ptr = reinterpret_cast<uint4*>(sQ + t * C::TILE + b * SUB + swz(r, c));
-          *ptr = rope8(*ptr, b * 64 + c * 8, pos, seg, p.rope_tab, off);
-        }
-      }
-      fence_proxy_async_smem();
-    }
-    if (ok) mbar_arrive(B.q_ready);
+    const uint32_t tP = C::SPEC ? tO + 64u : tS;  // packed bf16 probabilities
     const float sc = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; ok && j < nt; ++j) {
-      if (!mbar_wait(B.s_full + t, (uint32_t)j & 1u)) {
+    const float2 sc2 = make_float2(sc, sc);
+    int64_t u = u_lo;
+    int sg = 0, g = 0;  // segment and global tile counters (as the other roles count them)
+    bool ok = true;
+    while (ok && u < u_hi) {
+      // ---- start of an item: its queries
+      const int64_t item = u / nkt;
+      const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+      const int k0 = (int)(u - item * nkt), k1 = (int)(seg_hi - item * nkt);
+      const ItemPos ip = item_pos(p, item, npairs);
+      const int64_t row = ip.q0 + t * BM + r;
+      const int qb = sg % C::QB;
+      if (!mbar_wait(B.q_full + qb, (uint32_t)(sg / C::QB) & 1u)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float sv[BN / 32][32];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
-      int key0, nvalid;
-      key_tile(p, nt0, j, key0, nvalid);
-      if (nvalid < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
-      }
-      float mx[4] = {sv[0][0], sv[0][1], sv[0][2], sv[0][3]};
-#pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx[0] = fmaxf(mx[0], sv[c >> 5][c & 31]);
-        mx[1] = fmaxf(mx[1], sv[c >> 5][(c + 1) & 31]);
-        mx[2] = fmaxf(mx[2], sv[c >> 5][(c + 2) & 31]);
-        mx[3] = fmaxf(mx[3], sv[c >> 5][(c + 3) & 31]);
-      }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
-      const bool need = mt > m_run + kRescaleThreshold;
-      const float m_new = need ? mt : m_run;
-      const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-      // P = exp2(s*sc - m) as packed bf16 over the first 64 columns of S
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float e0 = fast_exp2(__fmaf_rn(sv[part][2 * q], sc, -m_new));
-          const float e1 = fast_exp2(__fmaf_rn(sv[part][2 * q + 1], sc, -m_new));
-          rs[(2 * q) & 3] += e0;
-          rs[(2 * q + 1) & 3] += e1;
-          pk[q] = pack_bf16x2(e0, e1);
+      if (p.rope_on && row < p.q_rows) {
+        const int tok = (int)(row % p.chunk_tokens);
+        const int jf = tok / p.tokens_L, l = tok % p.tokens_L;
+        const int pos[3] = {p.p0 + jf, l / p.grid_w, l % p.grid_w};
+        const int seg[3] = {p.rope_seg[0], p.rope_seg[1], p.rope_seg[2]};
+        const int off[3] = {p.tab_off[0], p.tab_off[1], p.tab_off[2]};
+        uint8_t* qt = sQ + (qb * 2 + t) * C::TILE;
+#pragma unroll 1
+        for (int b = 0; b < C::NSUB; ++b) {
+#pragma unroll 2
+          for (int c = 0; c < 8; ++c) {
+            uint4* ptr = reinterpret_cast<uint4*>(qt + b * SUB + swz(r, c));
+            *ptr = rope8(*ptr, b * 64 + c * 8, pos, seg, p.rope_tab, off);
+          }
         }
-        tmem_st16u(tS + (uint32_t)(part * 16), pk);
+        fence_proxy_async_smem();
       }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O may be rescaled only once the previous PV into it has landed
-        if (!mbar_wait(B.o_done + t, (uint32_t)(j - 1) & 1u)) {
+      mbar_arrive(B.q_ready + 2 * qb + t);
+      float m_run = -INFINITY, l_run = 0.f;
+      // ---- the item's key tiles
+      for (int kt = k0; kt < k1; ++kt, ++g) {
+        if (!mbar_wait(B.s_full + t, (uint32_t)g & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        float sv[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
+        int key0, nvalid;
+        key_tile(p, nt0, kt, key0, nvalid);
+        if (nvalid < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
+        }
+        // P = exp2(s*sc - m) as packed bf16 over the first 64 columns of S;
+        // returns the row sum of this tile's probabilities.  With WITH_MAX
+        // the tile's raw score max is accumulated into tmax on the way.
+        auto exp_pass = [&](float m, auto with_max, float& tmax) -> float {
+          constexpr bool WM = decltype(with_max)::value;
+          const float2 nm2 = make_float2(-m, -m);
+          float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int part = 0; part < 4; ++part) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float a0 = sv[part][2 * q], a1 = sv[part][2 * q + 1];
+              if (WM) mx[q & 3] = fmax3(mx[q & 3], a0, a1);
+              const float2 x = __ffma2_rn(make_float2(a0, a1), sc2, nm2);
+              const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+              rs[q & 3] = __fadd2_rn(rs[q & 3], make_float2(e0, e1));
+              pk[q] = pack_bf16x2(e0, e1);
+            }
+            tmem_st16u(tP + (uint32_t)(part * 16), pk);
+          }
+          if (WM) tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float2 s01 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+          return s01.x + s01.y;
+        };
+        float alpha = 1.f, m_new, lsum, tmax = -INFINITY;
+        auto row_max = [&]() {
+          float mx[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            mx[c] = sv[c][0];
+#pragma unroll
+            for (int i = 1; i < 31; i += 2) mx[c] = fmax3(mx[c], sv[c][i], sv[c][i + 1]);
+            mx[c] = fmaxf(mx[c], sv[c][31]);
+          }
+          return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+        };
+        bool rescale = false;
+        if (kt == k0) {
+          // first tile of the item: its own max first
+          m_new = row_max();
+          lsum = exp_pass(m_new, std::false_type{}, tmax);
+        } else if (C::SPEC) {
+          // against the running max, checking the tile max on the way
+          m_new = m_run;
+          lsum = exp_pass(m_run, std::true_type{}, tmax);
+          const float mt = tmax * sc;
+          const bool need = mt > m_run + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            if (need) {
+              m_new = mt;
+              alpha = fast_exp2(m_run - m_new);
+            }
+            // redo from S, which is still in tensor memory
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
+            if (nvalid < BN) {
+#pragma unroll
+              for (int c = 0; c < BN; ++c)
+                sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
+            }
+            tmem_wait_st();
+            lsum = exp_pass(m_new, std::false_type{}, tmax);
+            rescale = true;
+          }
+        } else {
+          const float mt = row_max();
+          const bool need = mt > m_run + kRescaleThreshold;
+          m_new = need ? mt : m_run;
+          alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+          lsum = exp_pass(m_new, std::false_type{}, tmax);
+          rescale = __any_sync(0xffffffffu, need);
+        }
+        if (rescale) {
+          // O may be rescaled only once the previous PV into it has landed
+          if (!mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float tmp[32];
+            tmem_ld32(tO + (uint32_t)(c * 32), tmp);
+            tmem_wait_ld();
+            reg_fence32(tmp);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) tmp[q] *= alpha;
+            tmem_st32(tO + (uint32_t)(c * 32), tmp);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(B.p_full + t);
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+      }
+      const int g_last = g - 1;
+      if (!ok) break;
+      // ---- end of the item's segment: O is complete once the last PV lands
+      if (!mbar_wait(B.o_done + t, (uint32_t)g_last & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      u = seg_hi;
+      ++sg;
+      if (k0 == 0 && k1 == nkt) {
+        const float inv = 1.f / l_run;
+        uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float tmp[32];
+          tmem_ld32(tO + (uint32_t)(c * 32), tmp);
+          tmem_wait_ld();
+          reg_fence32(tmp);
+          if (row < p.q_rows) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+              uint4 pk;
+              pk.x = pack_bf16x2(tmp[q + 0] * inv, tmp[q + 1] * inv);
+              pk.y = pack_bf16x2(tmp[q + 2] * inv, tmp[q + 3] * inv);
+              pk.z = pack_bf16x2(tmp[q + 4] * inv, tmp[q + 5] * inv);
+              pk.w = pack_bf16x2(tmp[q + 6] * inv, tmp[q + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
+            }
+          }
+        }
+      } else {
+        // partial: publish (O, m, l) of this row, count in, and merge if last
+        const int64_t slot = (item == u_lo / nkt) ? 0 : 1;
+        const int64_t rec = ((cta * 2 + slot) * 2 + t) * BM + r;
+        float* wo = p.ws_o + rec * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float tmp[32];
@@ -354,49 +633,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence32(tmp);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) tmp[q] *= alpha;
-          tmem_st32(tO + (uint32_t)(c * 32), tmp);
+          for (int q = 0; q < 32; q += 4)
+            __stcg(reinterpret_cast<float4*>(wo + c * 32 + q),
+                   make_float4(tmp[q], tmp[q + 1], tmp[q + 2], tmp[q + 3]));
         }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(B.p_full + t);
-      l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      m_run = m_new;
-    }
-    if (ok) ok = mbar_wait(B.o_done + t, (uint32_t)(nt - 1) & 1u);
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l_run;
-      uint16_t* orow = p.o + (((int64_t)s * p.q_rows + row) * p.H + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float tmp[32];
-        tmem_ld32(tO + (uint32_t)(c * 32), tmp);
-        tmem_wait_ld();
-        reg_fence32(tmp);
-        if (row < p.q_rows) {
-#pragma unroll
-          for (int q = 0; q < 32; q += 8) {
-            uint4 pk;
-            pk.x = pack_bf16x2(tmp[q + 0] * inv, tmp[q + 1] * inv);
-            pk.y = pack_bf16x2(tmp[q + 2] * inv, tmp[q + 3] * inv);
-            pk.z = pack_bf16x2(tmp[q + 4] * inv, tmp[q + 5] * inv);
-            pk.w = pack_bf16x2(tmp[q + 6] * inv, tmp[q + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
+        __stcg(p.ws_ml + rec, make_float2(m_run, l_run));
+        __threadfence();
+        const int64_t c_first = sp.owner(item * nkt), c_last = sp.owner((item + 1) * nkt - 1);
+        unsigned int* cnt = p.ws_cnt + (c_first * 2 + t) * BM + r;
+        const unsigned int prev = atomicAdd(cnt, 1u);
+        if (prev == (unsigned int)(c_last - c_first)) {
+          __threadfence();
+          float M = -INFINITY;
+          for (int64_t cc = c_first; cc <= c_last; ++cc) {
+            const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+            M = fmaxf(M, __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r).x);
           }
+          float Lsum = 0.f;
+          for (int64_t cc = c_first; cc <= c_last; ++cc) {
+            const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+            const float2 ml = __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r);
+            Lsum += ml.y * fast_exp2(ml.x - M);
+          }
+          const float inv = 1.f / Lsum;
+          uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+              const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+              const int64_t rc = ((cc * 2 + sl) * 2 + t) * BM + r;
+              const float w = fast_exp2(__ldcg(p.ws_ml + rc).x - M) * inv;
+              const float4* src = reinterpret_cast<const float4*>(p.ws_o + rc * D + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 v = __ldcg(src + q);
+                acc[4 * q + 0] = __fmaf_rn(v.x, w, acc[4 * q + 0]);
+                acc[4 * q + 1] = __fmaf_rn(v.y, w, acc[4 * q + 1]);
+                acc[4 * q + 2] = __fmaf_rn(v.z, w, acc[4 * q + 2]);
+                acc[4 * q + 3] = __fmaf_rn(v.w, w, acc[4 * q + 3]);
+              }
+            }
+            if (row < p.q_rows) {
+#pragma unroll
+              for (int q = 0; q < 32; q += 8) {
+                uint4 pk;
+                pk.x = pack_bf16x2(acc[q + 0], acc[q + 1]);
+                pk.y = pack_bf16x2(acc[q + 2], acc[q + 3]);
+                pk.z = pack_bf16x2(acc[q + 4], acc[q + 5]);
+                pk.w = pack_bf16x2(acc[q + 6], acc[q + 7]);
+                *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
+              }
+            }
+          }
+          *cnt = 0u;  // ready for the next launch
         }
       }
-    } else if (nt > 0) {
-      fail_wait(B);
     }
+    if (!ok) fail_wait(B);
   }
 
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *B.abort_flag && p.state)
-    atomicOr(reinterpret_cast<unsigned long long*>(&p.state[s].pub.error_word),
-             (unsigned long long)kErrAttnWaitTimeout);
+    for (int s = 0; s < p.S; ++s)
+      atomicOr(reinterpret_cast<unsigned long long*>(&p.state[s].pub.error_word),
+               (unsigned long long)kErrAttnWaitTimeout);
   if (wid == 9) {
     __syncwarp();
     tc_fence_after();
@@ -429,23 +733,53 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t hd, int64_t rows
 
 template <int D>
 static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnParams& p, int S, cudaStream_t st) {
+                            const AttnParams& p, int sm_count, cudaStream_t st) {
   const int smem = Cfg<D>::ALLOC;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
-  dim3 grid((unsigned)((p.q_rows + 2 * BM - 1) / (2 * BM)), (unsigned)p.H, (unsigned)S);
-  attn_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+  const int64_t nkt = (p.seg_count[0] + BN - 1) / BN + (p.seg_count[1] + BN - 1) / BN;
+  const int64_t items = (int64_t)p.S * p.H * ((p.q_rows + 2 * BM - 1) / (2 * BM));
+  if (nkt <= 0 || items <= 0) return cudaErrorInvalidValue;
+  // One CTA per item unless that leaves a poor last wave on a large
+  // problem; then the persistent split schedule (needs the workspace).
+  const int64_t sms = sm_count > 0 ? sm_count : 1;
+  const int64_t waves = (items + sms - 1) / sms;
+  const bool ragged = items * 10 < waves * sms * 9;  // last wave < 90 % full
+  const bool large = items * nkt >= 16 * sms;        // >= 16 key tiles per CTA
+  int64_t grid;
+  const bool has_ws = p.ws_o && p.ws_ml && p.ws_cnt;
+  if (has_ws && p.grid > 0) {
+    grid = p.grid;
+  } else if (has_ws && ragged && large) {
+    grid = sms;
+  } else {
+    grid = items;  // one item per CTA: nothing is split
+  }
+  if (has_ws) {
+    if (grid > kAttnMaxCtas && grid != items) grid = kAttnMaxCtas;
+    if (grid > items * nkt) grid = items * nkt;
+  } else {
+    grid = items;
+  }
+  if (grid < 1 || grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  attn_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int head_dim, int S, cudaStream_t st) {
-  if (head_dim == 64) return launch_d<64>(tq, tk, tv, p, S, st);
-  if (head_dim == 128) return launch_d<128>(tq, tk, tv, p, S, st);
+                             const AttnParams& p, int head_dim, int S, int sm_count,
+                             cudaStream_t st) {
+  if (p.S != S) return cudaErrorInvalidValue;
+  if (head_dim == 64) return launch_d<64>(tq, tk, tv, p, sm_count, st);
+  if (head_dim == 128) return launch_d<128>(tq, tk, tv, p, sm_count, st);
   return cudaErrorInvalidValue;
 }
 

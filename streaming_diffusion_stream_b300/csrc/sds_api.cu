@@ -28,6 +28,7 @@ struct sds_ctx {
   DevState* state = nullptr;  // [S]
   double* partials = nullptr;
   unsigned int* counters = nullptr;  // [1 + S]
+  void* attn_ws = nullptr;           // split-key workspace of the attention kernel
   std::vector<void*> allocs;
   // tables
   int rope_seg[3] = {0, 0, 0};
@@ -119,6 +120,7 @@ sds_status validate(const sds_config* c, std::string& why) {
       return bad("t_index entry maps outside the training schedule");
   }
   if (c->cfg_type != 0 && c->cfg_type != 1) return bad("cfg_type must be 0 (none) or 1 (self)");
+  if (c->attn_ctas < 0 || c->attn_ctas > kAttnMaxCtas) return bad("attn_ctas must be in [0, 160]");
   if (c->slot_elems < 4 || c->slot_elems % 4 != 0) return bad("slot_elems must be a positive multiple of 4");
   if (c->ssf_on) {
     if (c->ssf_elems < 4 || c->ssf_elems % 4 != 0) return bad("ssf_elems must be a positive multiple of 4");
@@ -216,9 +218,10 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   const int64_t ssf_ref = c.ssf_on ? 2 * S * c.ssf_elems : 0;
   const int64_t mot_prev = c.motion_on ? 2 * S * c.frame_elems : 0;
   const int64_t partials = S * nb_s * 3 + S * c.frames_T * nb_m;
+  const size_t ws_bytes = attn_ws_bytes((int)c.head_dim);
   const size_t bytes = (size_t)kv_elems * 2 * 2 + (size_t)emb * 4 + (size_t)tab_entries * 8 +
                        (size_t)ssf_ref * 4 + (size_t)mot_prev * 4 + (size_t)S * sizeof(DevState) +
-                       (size_t)partials * 8 + (size_t)(S + 1) * 4;
+                       (size_t)partials * 8 + (size_t)(S + 1) * 4 + ws_bytes;
   if (c.mem_cap_bytes > 0 && bytes > (size_t)c.mem_cap_bytes)
     return fail(nullptr, SDS_ERR_OOM, "context needs %zu bytes > mem_cap_bytes %lld", bytes,
                 (long long)c.mem_cap_bytes);
@@ -270,6 +273,7 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   ALLOC(ctx->state, S * (int64_t)sizeof(DevState));
   ALLOC(ctx->partials, partials * 8);
   ALLOC(ctx->counters, (S + 1) * 4);
+  ALLOC(ctx->attn_ws, ws_bytes);
 #undef ALLOC
 
   // RoPE table: angle pos * base^(-2i/w) in double, stored as fp32 (cos, sin)
@@ -425,7 +429,18 @@ sds_status sds_sink_refresh(sds_ctx* ctx, const float* chunk_emb, sds_stream_t s
 static sds_status attend_common(sds_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, AttnParams& ap, int head_dim, int S,
                                 cudaStream_t st) {
-  cudaError_t e = launch_attention(tq, tk, tv, ap, head_dim, S, st);
+  ap.S = S;
+  int sm_count = 0;
+  if (ctx) {
+    sm_count = ctx->sm_count;
+    const size_t per_rec = (size_t)kAttnMaxCtas * 2 * 2 * 128;
+    ap.ws_o = reinterpret_cast<float*>(ctx->attn_ws);
+    ap.ws_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ctx->attn_ws) + per_rec * head_dim * 4);
+    ap.ws_cnt = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ctx->attn_ws) +
+                                                per_rec * ((size_t)head_dim * 4 + 8));
+    ap.grid = (int32_t)ctx->cfg.attn_ctas;
+  }
+  cudaError_t e = launch_attention(tq, tk, tv, ap, head_dim, S, sm_count, st);
   if (e != cudaSuccess) {
     if (ctx) return cuda_fail(ctx, e, "attention launch");
     return fail(nullptr, SDS_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));

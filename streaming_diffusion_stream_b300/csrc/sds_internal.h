@@ -35,6 +35,7 @@ enum : int64_t {
 struct AttnParams {
   uint16_t* o;           // bf16 [S][q_rows][H][d]
   int64_t q_rows;        // query rows per stream
+  int32_t S;             // independent problems (streams)
   int32_t H;
   int32_t seg_start[2];  // key row ranges inside the K/V tensor of a stream
   int32_t seg_count[2];
@@ -46,11 +47,27 @@ struct AttnParams {
   const float2* rope_tab;
   int32_t tab_off[3];    // entry offset of each axis table
   DevState* state;       // per stream, for error reporting (may be null)
+  // Split-key workspace of the persistent schedule.  Null: one work item
+  // (a pair of 128-row query tiles of one stream and head, all keys) per
+  // CTA, nothing is split.  Otherwise a grid of at most kAttnMaxCtas CTAs
+  // divides the (item, key tile) units evenly; an item whose keys are split
+  // between CTAs is finished by the last contributor to arrive.
+  float* ws_o;           // [kAttnMaxCtas][2 slots][2 tiles][128 rows][d] partial O, fp32
+  float2* ws_ml;         // [kAttnMaxCtas][2][2][128] partial (running max, sum)
+  unsigned int* ws_cnt;  // [kAttnMaxCtas][2][128] arrival counters, zero between launches
+  int32_t grid;          // CTAs of the persistent schedule (0: the device's SM count)
 };
+
+constexpr int kAttnMaxCtas = 160;  // >= the SM count of the target part (148)
+// Bytes of the split-key workspace for head_dim d.
+inline size_t attn_ws_bytes(int d) {
+  return (size_t)kAttnMaxCtas * 2 * 2 * 128 * ((size_t)d * 4 + 8) + (size_t)kAttnMaxCtas * 2 * 128 * 4;
+}
 
 // q/k/v tensor maps: 3-D {H*d, rows, S}, box {64, 128, 1}, 128-byte swizzle.
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int head_dim, int S, cudaStream_t st);
+                             const AttnParams& p, int head_dim, int S, int sm_count,
+                             cudaStream_t st);
 
 // Build a bf16 3-D tensor map {H*d, rows, S} with a {64, 128, 1} box.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t hd, int64_t rows, int64_t S);

@@ -72,6 +72,29 @@ def test_image_mode_attend_small_batch():
         g.close()
 
 
+@pytest.mark.parametrize("ctas,L,H", [
+    (7, 320, 5),     # items split across many CTAs, several contributors each
+    (37, 320, 5),    # ragged split points
+    (148, 320, 5),   # more CTAs than items
+    (160, 96, 2),    # one query pair, keys split into single tiles
+])
+def test_image_mode_split_key_schedule(ctas, L, H):
+    """The persistent schedule with keys of a query tile split between CTAs
+    (partials merged by the last contributor) against the oracle."""
+    w = W.get_config("c2_sdturbo_image", L=L, H=H, grid_h=16, grid_w=L // 16, latent_h=16,
+                     latent_w=L // 16, ssf_h=64, ssf_w=64, attn_ctas=ctas)
+    g = GpuPipe(w)
+    try:
+        for rep in range(2):  # the second launch reuses the arrival counters
+            q = W.gen_q(w, rep)
+            k, v = W.gen_kv(w, rep)
+            got = g.attend(q, k, v)
+            ref = O.attention(q[0], k[0], v[0])
+            assert attn_rel_err(got[0], ref) <= TOL, (ctas, rep)
+    finally:
+        g.close()
+
+
 def test_image_mode_full_size_sampled_rows():
     """c2 at full size (4 slots x 4096 queries against 16384 batch keys), sampled rows."""
     w = W.get_config("c2_sdturbo_image")

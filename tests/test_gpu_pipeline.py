@@ -140,6 +140,13 @@ def test_c1_two_streams():
     run_sequence(w, 6)
 
 
+def test_c1_split_key_schedule_with_sink_fill():
+    """Video mode on the persistent split schedule (keys of each query tile
+    split between CTAs), through sink fill, refresh and ring wrap."""
+    w = W.get_config("c1_tiny", M=2, T=3, R=6, mot_k=3, emb_step=0.5, attn_ctas=5)
+    run_sequence(w, 6)
+
+
 def test_rope_reset_fires_with_small_tau():
     w = W.get_config("c1_tiny", rope_tau=3, steps=11)
     stats = run_sequence(w, 11)
