@@ -85,7 +85,9 @@ def step_bytes(w: dict, with_ssf: bool, with_motion: bool) -> float:
 
 
 def push_bytes(w: dict) -> float:
-    return 2.0 * 2 * w["streams"] * w["kv_rows"] * w["HD"]  # K and V, read + write
+    """Algorithmic bytes of one K2 launch: the chunk's K and V read once and
+    written once into the ring (bf16)."""
+    return 2.0 * 4 * w["streams"] * w["kv_rows"] * w["HD"]
 
 
 def load_peaks() -> dict:
@@ -198,9 +200,11 @@ class Runner:
         # pool of independent input sets larger than L2
         set_bytes = self.set_bytes()
         self.n_sets = int(max(2, min(64, np.ceil(pool_bytes_min / set_bytes))))
+        # consecutive chunk embeddings are steps of one unit-norm random walk,
+        # as in the workload (the sink refreshes when the walk drifts past s_th)
+        self.emb_walk = W.EmbeddingWalk(w)
         self.sets = [self.make_set(i) for i in range(self.n_sets)]
         self.pool_bytes = set_bytes * self.n_sets
-        self.emb_walk = W.EmbeddingWalk(w)
 
     def set_bytes(self) -> float:
         w = self.w
@@ -226,7 +230,7 @@ class Runner:
         if w["motion"]:
             d["chunk"] = W.LatentWalk(dict(w, seed=w["seed"] + 104729 * (i + 1))).next()
         if self.video and w["M"] > 0:
-            d["h"] = W.EmbeddingWalk(dict(w, seed=w["seed"] + 31 * (i + 1))).next()
+            d["h"] = self.emb_walk.next()
         return d
 
     def make_set(self, i: int) -> dict:

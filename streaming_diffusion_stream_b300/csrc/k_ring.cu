@@ -8,6 +8,7 @@
 // Both kernels stream 16-byte vectors with consecutive threads on
 // consecutive addresses; there is no shared-memory staging because every
 // byte is read once and written once.
+#include "dfloat.cuh"
 #include "rope.cuh"
 #include "sds_internal.h"
 
@@ -15,62 +16,109 @@ namespace sds {
 namespace {
 
 constexpr int kRingThreads = 256;
+constexpr int kPushX = 64;  // threads along a token row (a multiple of head_dim / 8)
+constexpr int kPushY = 4;   // token rows per block
 
-__global__ void __launch_bounds__(kRingThreads) kv_push_kernel(const PushParams p) {
-  const int64_t vpr = p.HD / 8;  // vectors per token row
-  const int64_t TL = p.T * p.L;
-  const int64_t total = p.S * TL * vpr;
+// One block of kPushX x kPushY threads moves kPushY token rows at a time
+// (grid-stride over the S*T*L rows of the chunk).  Thread x of a row handles
+// vectors x, x + 64, x + 128, ... of the row; since 64 is a multiple of the
+// eight-element vectors per head, all of them sit at the same offset inside
+// their heads and share one set of RoPE (cos, sin) pairs, which the thread
+// fetches once per row.  Index arithmetic is 32-bit per row.
+__global__ void __launch_bounds__(kPushX * kPushY) kv_push_kernel(const PushParams p) {
+  const int vpr = (int)(p.HD / 8);  // vectors per token row
+  const int TL = (int)(p.T * p.L);
+  const int64_t rows = p.S * TL;
   const int64_t kv_rows = (p.M + p.R) * p.L;
-  const int seg[3] = {p.rope_seg[0], p.rope_seg[1], p.rope_seg[2]};
-  const int off[3] = {p.tab_off[0], p.tab_off[1], p.tab_off[2]};
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t vr = i % vpr;
-    const int64_t row = i / vpr;
-    const int64_t tok = row % TL, s = row / TL;
-    const int64_t j = tok / p.L, l = tok % p.L;
+  const int x = threadIdx.x;
+  for (int64_t row = (int64_t)blockIdx.x * kPushY + threadIdx.y; row < rows;
+       row += (int64_t)gridDim.x * kPushY) {
+    const int s = (int)(row / TL);
+    const int tok = (int)(row - (int64_t)s * TL);
+    const int j = tok / (int)p.L, l = tok - j * (int)p.L;
     const int64_t slot = (p.F + j) % p.R;
-    const int64_t dst = (s * kv_rows + (p.M + slot) * p.L + l) * vpr + vr;
-    uint4 kv = __ldcs(p.k_in + i);
-    const uint4 vv = __ldcs(p.v_in + i);
+    const uint4* kin = p.k_in + row * vpr;
+    const uint4* vin = p.v_in + row * vpr;
+    uint4* kout = p.kv_k + ((int64_t)s * kv_rows + (p.M + slot) * p.L + l) * vpr;
+    uint4* vout = p.kv_v + ((int64_t)s * kv_rows + (p.M + slot) * p.L + l) * vpr;
+    float2 cs[4];
     if (p.rope_on) {
-      const int pos[3] = {p.p0 + (int)j, (int)(l / p.grid_w), (int)(l % p.grid_w)};
-      const int e0 = (int)((vr * 8) % p.head_dim);
-      kv = rope8(kv, e0, pos, seg, p.rope_tab, off);
+      const int pos[3] = {p.p0 + j, l / p.grid_w, l % p.grid_w};
+      const int h0 = p.rope_seg[0] >> 1, h1 = (p.rope_seg[0] + p.rope_seg[1]) >> 1;
+      const int pair0 = (int)(((int64_t)x * 8 % p.head_dim) >> 1);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pair = pair0 + q;
+        const bool a0 = pair < h0, a1 = !a0 && pair < h1;
+        const int i = a0 ? pair : (a1 ? pair - h0 : pair - h1);
+        const int base = a0 ? p.tab_off[0] + pos[0] * h0
+                            : (a1 ? p.tab_off[1] + pos[1] * (p.rope_seg[1] >> 1)
+                                  : p.tab_off[2] + pos[2] * (p.rope_seg[2] >> 1));
+        cs[q] = p.rope_tab[base + i];
+      }
     }
-    p.kv_k[dst] = kv;
-    p.kv_v[dst] = vv;
+    int v = x;
+    for (; v + kPushX < vpr; v += 2 * kPushX) {
+      uint4 k0 = __ldcs(kin + v), k1 = __ldcs(kin + v + kPushX);
+      const uint4 v0 = __ldcs(vin + v), v1 = __ldcs(vin + v + kPushX);
+      if (p.rope_on) {
+        k0 = rope8_cs(k0, cs);
+        k1 = rope8_cs(k1, cs);
+      }
+      kout[v] = k0;
+      kout[v + kPushX] = k1;
+      vout[v] = v0;
+      vout[v + kPushX] = v1;
+    }
+    if (v < vpr) {
+      uint4 k0 = __ldcs(kin + v);
+      const uint4 v0 = __ldcs(vin + v);
+      if (p.rope_on) k0 = rope8_cs(k0, cs);
+      kout[v] = k0;
+      vout[v] = v0;
+    }
   }
 }
 
-__device__ __forceinline__ double warp_sum(double v) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Fixed-order block sum (valid in every thread after return).
-__device__ double block_sum_all(double v, double* red) {
-  v = warp_sum(v);
+// Fixed-order block sum of one compensated value per thread: a butterfly
+// in each warp, then thread 0 adds the warps in index order and converts
+// to double once; the result is returned to every thread.
+__device__ double block_sum_df(dfloat v, dfloat* red, double* out) {
+  v = df_warp_sum(v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  double r = 0.0;
-  for (int w = 0; w < kRingThreads / 32; ++w) r += red[w];
+  if (threadIdx.x == 0) {
+    dfloat t = red[0];
+    for (int w = 1; w < kRingThreads / 32; ++w) t = df_add(t, red[w]);
+    *out = df_to_double(t);
+  }
   __syncthreads();
-  return r;
+  return *out;
 }
 
 // Copy one frame (L tokens of all heads, K and V) between rows of a stream's
-// K/V buffer; this block's share of the vectors.
+// K/V buffer; this block's share of the vectors, four loads in flight per
+// thread before the stores.
 __device__ void copy_frame(const SinkParams& p, int64_t s, int64_t src_row0, int64_t dst_row0) {
   const int64_t vpr = p.HD / 8;
   const int64_t kv_rows = (p.M + p.R) * p.L;
   const int64_t n = p.L * vpr;
   const int64_t src = (s * kv_rows + src_row0) * vpr, dst = (s * kv_rows + dst_row0) * vpr;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    p.kv_k[dst + i] = p.kv_k[src + i];
-    p.kv_v[dst + i] = p.kv_v[src + i];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + stride < n; i += 2 * stride) {
+    const uint4 k0 = p.kv_k[src + i], k1 = p.kv_k[src + i + stride];
+    const uint4 v0 = p.kv_v[src + i], v1 = p.kv_v[src + i + stride];
+    p.kv_k[dst + i] = k0;
+    p.kv_k[dst + i + stride] = k1;
+    p.kv_v[dst + i] = v0;
+    p.kv_v[dst + i + stride] = v1;
+  }
+  if (i < n) {
+    const uint4 k0 = p.kv_k[src + i], v0 = p.kv_v[src + i];
+    p.kv_k[dst + i] = k0;
+    p.kv_v[dst + i] = v0;
   }
 }
 
@@ -80,7 +128,8 @@ __device__ void copy_frame(const SinkParams& p, int64_t s, int64_t src_row0, int
 // finishes last for the stream updates the embedding and the record -- so
 // no block can read an embedding another block already replaced.
 __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) {
-  __shared__ double red[kRingThreads / 32];
+  __shared__ dfloat red[kRingThreads / 32];
+  __shared__ double bcast;
   __shared__ int last;
   const int64_t s = blockIdx.y;
   const float* h = p.h + s * p.D;
@@ -103,21 +152,23 @@ __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) 
     }
     return;
   }
-  double hn = 0.0;
-  for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) hn += (double)h[t] * (double)h[t];
-  hn = block_sum_all(hn, red);
+  // Each thread sums its exact products as compensated fp32 pairs (fp64 is
+  // slow on this part); the block tree runs in double.
+  dfloat hn_t = df_make(0.f);
+  for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) hn_t = df_add(hn_t, df_prod(h[t], h[t]));
+  const double hn = block_sum_df(hn_t, red, &bcast);
   int64_t jstar = -1;
   double amin = __longlong_as_double(0x7FF0000000000000ll), a2 = amin;
   for (int64_t j = 0; j < p.M; ++j) {
     const float* e = p.emb + (s * p.M + j) * p.D;
-    double dot = 0.0, en = 0.0;
+    dfloat dot_t = df_make(0.f), en_t = df_make(0.f);
     for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) {
-      const double ev = (double)e[t];
-      dot += (double)h[t] * ev;
-      en += ev * ev;
+      const float ev = e[t];
+      dot_t = df_add(dot_t, df_prod(h[t], ev));
+      en_t = df_add(en_t, df_prod(ev, ev));
     }
-    dot = block_sum_all(dot, red);
-    en = block_sum_all(en, red);
+    const double dot = block_sum_df(dot_t, red, &bcast);
+    const double en = block_sum_df(en_t, red, &bcast);
     const double a = (hn > 0.0 && en > 0.0) ? dot / sqrt(hn * en) : 0.0;
     if (a < amin) {
       a2 = amin;
@@ -155,12 +206,15 @@ __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) 
 }  // namespace
 
 cudaError_t launch_kv_push(const PushParams& p, int sm_count, cudaStream_t st) {
-  const int64_t total = p.S * p.T * p.L * (p.HD / 8);
-  int64_t blocks = (total + kRingThreads - 1) / kRingThreads;
+  // the thread-to-vector mapping needs the row width to be a multiple of a
+  // head and a head to divide the 64-thread row stride
+  if (p.HD % 8 != 0 || (p.head_dim != 64 && p.head_dim != 128)) return cudaErrorInvalidValue;
+  const int64_t rows = p.S * p.T * p.L;
+  int64_t blocks = (rows + kPushY - 1) / kPushY;
   const int64_t cap = (int64_t)sm_count * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  kv_push_kernel<<<(int)blocks, kRingThreads, 0, st>>>(p);
+  kv_push_kernel<<<(int)blocks, dim3(kPushX, kPushY), 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,8 @@
 //       (StreamDiffusion notes, "Stream Batch"; blog section 7's ancestral
 //       step read as predict-x0-then-re-noise): x0hat, re-noise to the next
 //       slot's level with the supplied z, and noise the incoming frame into
-//       slot 0.  Slots are visited last-to-first so x_next may alias x.
+//       slot 0.  All of an element's inputs are loaded before any of its
+//       outputs is written, so x_next may alias x.
 //  (ii) StreamDiffusion notes, "Stochastic Similarity Filter": dot and norm
 //       sums of the incoming frame against the reference frame; the frame is
 //       also copied into the spare reference buffer, which becomes current
@@ -16,12 +17,16 @@
 //  (iii) StreamDiffusionV2 summary, "Motion-aware noise scheduler": sums of
 //       squared differences of consecutive latent frames.
 //
-// Reductions are deterministic: every work block (2048 elements) reduces in
-// a fixed order (fp32 over the thread's 8 elements, double beyond), writes
-// one partial per quantity, and the block that finishes last sums the
-// partials in index order in double and takes the decisions.  dot, |I|^2 and
+// Reductions are deterministic: every work block (8192 elements) reduces in
+// a fixed order (fp32 over 8 elements of a thread, compensated fp32 pairs
+// across threads, since fp64 is slow on this part) and writes one partial
+// per quantity.  Reduction work blocks are scheduled before update work
+// blocks; the one that completes the set of partials (an arrival counter)
+// sums them in a fixed order in double (one warp per sum) and takes the
+// decisions (one thread per stream) while the update streams on.  dot, |I|^2 and
 // |R|^2 use the same operation sequence, so identical frames give three
 // bitwise-equal sums, cosine exactly 1 and skip probability exactly 1.
+#include "dfloat.cuh"
 #include "sds_internal.h"
 
 namespace sds {
@@ -34,18 +39,31 @@ __device__ __forceinline__ double warp_sum(double v) {
 
 constexpr int kWarps = kStepThreads / 32;
 
-// Block-wide fixed-order sum of one double per thread; result valid in thread 0.
-__device__ __forceinline__ double block_sum(double v, double* red) {
-  v = warp_sum(v);
+// Block-wide fixed-order sums of three compensated values per thread
+// (butterfly within each warp, then the warps in index order); the results
+// are valid in thread 0.
+__device__ __forceinline__ void block_sum3(dfloat& a, dfloat& b, dfloat& c, dfloat* red) {
+  a = df_warp_sum(a);
+  b = df_warp_sum(b);
+  c = df_warp_sum(c);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  double r = 0.0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w) r += red[w];
+  if (lane == 0) {
+    red[warp] = a;
+    red[kWarps + warp] = b;
+    red[2 * kWarps + warp] = c;
   }
   __syncthreads();
-  return r;
+  if (threadIdx.x == 0) {
+    a = red[0];
+    b = red[kWarps];
+    c = red[2 * kWarps];
+    for (int w = 1; w < kWarps; ++w) {
+      a = df_add(a, red[w]);
+      b = df_add(b, red[kWarps + w]);
+      c = df_add(c, red[2 * kWarps + w]);
+    }
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ float4 ld4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
@@ -72,54 +90,89 @@ __device__ __forceinline__ float4 noise4(float4 a, float4 b, float ca, float cb)
                      __fmaf_rn(ca, a.z, cb * b.z), __fmaf_rn(ca, a.w, cb * b.w));
 }
 
+// One float4 column of every slot: all loads are issued before any store,
+// so the update may run in place (x_next[i] aliasing x[i]) and up to
+// 3N+1 16-byte loads per thread are in flight at once.
+template <int N>
 __device__ void update_block(const StepParams& p, int64_t w) {
-  const int64_t s = w / p.nb_u, b = w % p.nb_u;
-  const int64_t sbase = s * p.N_s;
-  for (int k = 0; k < 2; ++k) {
-    const int64_t el = b * kStepBlockElems + k * (kStepThreads * 4) + threadIdx.x * 4;
-    if (el >= p.N_s) continue;
-    const int64_t e = sbase + el;
-    for (int i = p.n - 1; i >= 0; --i) {
-      const float4 xh = x0hat4(ld4(p.x[i] + e), ld4(p.x0[i] + e), ld4(p.eps_c[i] + e), p, i);
-      if (i == p.n - 1) {
-        st4(p.out + e, xh);
-      } else {
-        st4(p.x_next[i + 1] + e, noise4(xh, ld4(p.z[i] + e), p.c_sa[i + 1], p.c_s1a[i + 1]));
-      }
-    }
-    st4(p.x_next[0] + e, noise4(ld4(p.x0_new + e), ld4(p.eps_new + e), p.c_sa[0], p.c_s1a[0]));
+  const int64_t s = w / p.nb_u, b = w - s * p.nb_u;
+  const int64_t el = b * kUpdBlockElems + threadIdx.x * 4;
+  if (el >= p.N_s) return;
+  const int64_t e = s * p.N_s + el;
+  float4 x[N], x0[N], ec[N], z[N > 1 ? N - 1 : 1];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    x[i] = ld4(p.x[i] + e);
+    x0[i] = ld4(p.x0[i] + e);
+    ec[i] = ld4(p.eps_c[i] + e);
+    if (i < N - 1) z[i] = ld4(p.z[i] + e);
   }
+  const float4 xn = ld4(p.x0_new + e), en = ld4(p.eps_new + e);
+#pragma unroll
+  for (int i = N - 1; i >= 0; --i) {
+    const float4 xh = x0hat4(x[i], x0[i], ec[i], p, i);
+    if (i == N - 1) {
+      st4(p.out + e, xh);
+    } else {
+      st4(p.x_next[i + 1] + e, noise4(xh, z[i], p.c_sa[i + 1], p.c_s1a[i + 1]));
+    }
+  }
+  st4(p.x_next[0] + e, noise4(xn, en, p.c_sa[0], p.c_s1a[0]));
 }
 
-__device__ void ssf_block(const StepParams& p, int64_t w, double* red) {
+// SSF and motion work blocks cover kRedBlockElems elements: 8 float4 per
+// array per thread, all loads in flight before any arithmetic.  Each thread
+// sums in fp32 over 8 consecutive elements of its own (two float4) and in
+// double beyond.
+constexpr int kRedVec = kRedBlockElems / (kStepThreads * 4);  // float4 per thread per array
+
+__device__ void ssf_block(const StepParams& p, int64_t w, dfloat* red) {
   const int64_t s = w / p.nb_s, b = w % p.nb_s;
   const int64_t cur = p.state[s].ssf_cur;
   const float* I = p.ssf_frame + s * p.E;
   const float* R = p.ssf_ref + (cur * p.S + s) * p.E;
   float* Rn = p.ssf_ref + ((cur ^ 1) * p.S + s) * p.E;
-  float dot = 0.f, ni = 0.f, nr = 0.f;
-  for (int k = 0; k < 2; ++k) {
-    const int64_t e = b * kStepBlockElems + k * (kStepThreads * 4) + threadIdx.x * 4;
-    if (e >= p.E) continue;
-    const float4 a = ld4(I + e), r = ld4(R + e);
-    st4(Rn + e, a);
-    dot = __fmaf_rn(a.x, r.x, dot); ni = __fmaf_rn(a.x, a.x, ni); nr = __fmaf_rn(r.x, r.x, nr);
-    dot = __fmaf_rn(a.y, r.y, dot); ni = __fmaf_rn(a.y, a.y, ni); nr = __fmaf_rn(r.y, r.y, nr);
-    dot = __fmaf_rn(a.z, r.z, dot); ni = __fmaf_rn(a.z, a.z, ni); nr = __fmaf_rn(r.z, r.z, nr);
-    dot = __fmaf_rn(a.w, r.w, dot); ni = __fmaf_rn(a.w, a.w, ni); nr = __fmaf_rn(r.w, r.w, nr);
+  const int64_t base = b * kRedBlockElems + threadIdx.x * 4;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 a[kRedVec], r[kRedVec];
+#pragma unroll
+  for (int k = 0; k < kRedVec; ++k) {
+    const int64_t e = base + k * (kStepThreads * 4);
+    const bool h = e < p.E;
+    a[k] = h ? ld4(I + e) : z4;
+    r[k] = h ? ld4(R + e) : z4;
   }
-  const double sd = block_sum((double)dot, red);
-  const double si = block_sum((double)ni, red);
-  const double sr = block_sum((double)nr, red);
+#pragma unroll
+  for (int k = 0; k < kRedVec; ++k) {
+    const int64_t e = base + k * (kStepThreads * 4);
+    if (e < p.E) st4(Rn + e, a[k]);
+  }
+  dfloat sd = df_make(0.f), si = df_make(0.f), sr = df_make(0.f);
+#pragma unroll
+  for (int k = 0; k < kRedVec; k += 2) {
+    float dot = 0.f, ni = 0.f, nr = 0.f;
+#pragma unroll
+    for (int k2 = k; k2 < k + 2; ++k2) {
+      const float4 x = a[k2], y = r[k2];
+      dot = __fmaf_rn(x.x, y.x, dot); ni = __fmaf_rn(x.x, x.x, ni); nr = __fmaf_rn(y.x, y.x, nr);
+      dot = __fmaf_rn(x.y, y.y, dot); ni = __fmaf_rn(x.y, x.y, ni); nr = __fmaf_rn(y.y, y.y, nr);
+      dot = __fmaf_rn(x.z, y.z, dot); ni = __fmaf_rn(x.z, x.z, ni); nr = __fmaf_rn(y.z, y.z, nr);
+      dot = __fmaf_rn(x.w, y.w, dot); ni = __fmaf_rn(x.w, x.w, ni); nr = __fmaf_rn(y.w, y.w, nr);
+    }
+    sd = df_add(sd, df_make(dot));
+    si = df_add(si, df_make(ni));
+    sr = df_add(sr, df_make(nr));
+  }
+  block_sum3(sd, si, sr, red);
   if (threadIdx.x == 0) {
     double* part = p.partials + (s * p.nb_s + b) * 3;
-    part[0] = sd;
-    part[1] = si;
-    part[2] = sr;
+    part[0] = df_to_double(sd);
+    part[1] = df_to_double(si);
+    part[2] = df_to_double(sr);
   }
 }
 
-__device__ void motion_block(const StepParams& p, int64_t w, double* red) {
+__device__ void motion_block(const StepParams& p, int64_t w, dfloat* red) {
   const int64_t per_s = p.T * p.nb_m;
   const int64_t s = w / per_s, rem = w % per_s, j = rem / p.nb_m, b = rem % p.nb_m;
   const float* B = p.mot_chunk + (s * p.T + j) * p.N_f;
@@ -129,126 +182,183 @@ __device__ void motion_block(const StepParams& p, int64_t w, double* red) {
   } else if (p.state[s].mot_has_prev) {
     A = p.mot_prev_in + s * p.N_f;
   }
-  float acc = 0.f;
-  for (int k = 0; k < 2; ++k) {
-    const int64_t e = b * kStepBlockElems + k * (kStepThreads * 4) + threadIdx.x * 4;
-    if (e >= p.N_f) continue;
-    const float4 bv = ld4(B + e);
-    if (j == p.T - 1) st4(p.mot_prev_out + s * p.N_f + e, bv);
-    if (A) {
-      const float4 av = ld4(A + e);
-      const float dx = bv.x - av.x, dy = bv.y - av.y, dz = bv.z - av.z, dw = bv.w - av.w;
-      acc = __fmaf_rn(dx, dx, acc);
-      acc = __fmaf_rn(dy, dy, acc);
-      acc = __fmaf_rn(dz, dz, acc);
-      acc = __fmaf_rn(dw, dw, acc);
+  const int64_t base = b * kRedBlockElems + threadIdx.x * 4;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 bv[kRedVec], av[kRedVec];
+#pragma unroll
+  for (int k = 0; k < kRedVec; ++k) {
+    const int64_t e = base + k * (kStepThreads * 4);
+    const bool h = e < p.N_f;
+    bv[k] = h ? ld4(B + e) : z4;
+    av[k] = (h && A) ? ld4(A + e) : z4;
+  }
+  if (j == p.T - 1) {
+#pragma unroll
+    for (int k = 0; k < kRedVec; ++k) {
+      const int64_t e = base + k * (kStepThreads * 4);
+      if (e < p.N_f) st4(p.mot_prev_out + s * p.N_f + e, bv[k]);
     }
   }
-  const double sa = block_sum((double)acc, red);
-  if (threadIdx.x == 0) p.partials[p.S * p.nb_s * 3 + (s * p.T + j) * p.nb_m + b] = sa;
+  dfloat sq = df_make(0.f), unused1 = df_make(0.f), unused2 = df_make(0.f);
+  if (A) {
+#pragma unroll
+    for (int k = 0; k < kRedVec; k += 2) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k2 = k; k2 < k + 2; ++k2) {
+        const float dx = bv[k2].x - av[k2].x, dy = bv[k2].y - av[k2].y;
+        const float dz = bv[k2].z - av[k2].z, dw = bv[k2].w - av[k2].w;
+        acc = __fmaf_rn(dx, dx, acc);
+        acc = __fmaf_rn(dy, dy, acc);
+        acc = __fmaf_rn(dz, dz, acc);
+        acc = __fmaf_rn(dw, dw, acc);
+      }
+      sq = df_add(sq, df_make(acc));
+    }
+  }
+  block_sum3(sq, unused1, unused2, red);
+  if (threadIdx.x == 0) p.partials[p.S * p.nb_s * 3 + (s * p.T + j) * p.nb_m + b] = df_to_double(sq);
 }
 
-// Fixed-order sum of n partials at stride `stride` (thread-strided, then block tree).
-__device__ double sum_partials(const double* base, int64_t n, int64_t stride, double* red) {
-  double v = 0.0;
-  for (int64_t i = threadIdx.x; i < n; i += kStepThreads) v += __ldcg(base + i * stride);
-  return block_sum(v, red);
-}
+constexpr int kFinChunk = 32;  // streams finished per round of the last block
+constexpr int kFinPer = 3 + SDS_MAX_CHUNK_FRAMES;  // sums per stream at most
 
-__device__ void finalize(const StepParams& p, double* red) {
-  for (int64_t s = 0; s < p.S; ++s) {
-    DevState* st = p.state + s;
-    if (p.ssf_frame) {
-      const double* base = p.partials + s * p.nb_s * 3;
-      const double dot = sum_partials(base + 0, p.nb_s, 3, red);
-      const double ni = sum_partials(base + 1, p.nb_s, 3, red);
-      const double nr = sum_partials(base + 2, p.nb_s, 3, red);
-      if (threadIdx.x == 0) {
-        double cosv = 0.0, P = 0.0;
-        int64_t skip = 0;
-        if (st->pub.ssf_has_ref) {
-          cosv = (ni > 0.0 && nr > 0.0) ? dot / sqrt(ni * nr) : 0.0;
-          P = fmin(1.0, fmax(0.0, (cosv - p.eta) / (1.0 - p.eta)));
-          const double u = (double)__ldcg(p.ssf_u + s);
-          skip = (u < P && st->pub.ssf_skip_count < p.max_skip) ? 1 : 0;
-        }
-        if (skip) {
-          st->pub.ssf_skip_count += 1;
-        } else {
-          st->pub.ssf_skip_count = 0;
-          st->ssf_cur ^= 1;
-          st->pub.ssf_has_ref = 1;
-        }
-        st->pub.ssf_skip = skip;
-        st->pub.ssf_cos = cosv;
-        st->pub.ssf_p = P;
-        st->pub.ssf_evals += 1;
-      }
+// The SSF decision and the motion / noise-rate update of stream s from its
+// reduced sums (dot, |I|^2, |R|^2, then one squared difference per pair).
+// The record's fields are read in one batch of independent loads, updated
+// in registers and written back, so the chain of dependent global-memory
+// round trips stays short.
+__device__ void decide(const StepParams& p, int64_t s, const double* sums) {
+  DevState* st = p.state + s;
+  if (p.ssf_frame) {
+    const int64_t has_ref = st->pub.ssf_has_ref, count = st->pub.ssf_skip_count;
+    const int64_t cur = st->ssf_cur, evals = st->pub.ssf_evals;
+    const double u = (double)__ldcg(p.ssf_u + s);
+    const double dot = sums[0], ni = sums[1], nr = sums[2];
+    double cosv = 0.0, P = 0.0;
+    int64_t skip = 0;
+    if (has_ref) {
+      cosv = (ni > 0.0 && nr > 0.0) ? dot / sqrt(ni * nr) : 0.0;
+      P = fmin(1.0, fmax(0.0, (cosv - p.eta) / (1.0 - p.eta)));
+      skip = (u < P && count < p.max_skip) ? 1 : 0;
     }
-    if (p.mot_chunk) {
-      const double* base = p.partials + p.S * p.nb_s * 3 + s * p.T * p.nb_m;
-      for (int64_t j = 0; j < p.T; ++j) {
-        const double sq = sum_partials(base + j * p.nb_m, p.nb_m, 1, red);
-        if (threadIdx.x == 0) {
-          const bool present = (j > 0) || (st->mot_has_prev != 0);
-          double dv = __longlong_as_double(0x7FF8000000000000ll);  // NaN: pair absent
-          if (present) {
-            dv = sqrt(sq / (double)p.N_f);
-            st->mot_window[st->mot_head] = dv;
-            st->mot_head = (st->mot_head + 1) % p.mot_k;
-            if (st->mot_count < p.mot_k) st->mot_count += 1;
-            st->pub.motion_pairs += 1;
-          }
-          if (j < SDS_MAX_CHUNK_FRAMES) st->pub.motion_d[j] = dv;
-        }
+    st->pub.ssf_skip_count = skip ? count + 1 : 0;
+    st->ssf_cur = skip ? cur : (cur ^ 1);
+    st->pub.ssf_has_ref = skip ? has_ref : 1;
+    st->pub.ssf_skip = skip;
+    st->pub.ssf_cos = cosv;
+    st->pub.ssf_p = P;
+    st->pub.ssf_evals = evals + 1;
+    sums += 3;
+  }
+  if (p.mot_chunk) {
+    const int64_t has_prev = st->mot_has_prev;
+    int64_t head = st->mot_head, count = st->mot_count, pairs = st->pub.motion_pairs;
+    const double rate = st->pub.noise_rate, dhat_old = st->pub.motion_dhat;
+    const double nan = __longlong_as_double(0x7FF8000000000000ll);  // pair absent
+    for (int64_t j = 0; j < p.T; ++j) {
+      const bool present = (j > 0) || (has_prev != 0);
+      double dv = nan;
+      if (present) {
+        dv = sqrt(sums[j] / (double)p.N_f);
+        st->mot_window[head] = dv;
+        head = (head + 1) % p.mot_k;
+        if (count < p.mot_k) count += 1;
+        pairs += 1;
       }
-      if (threadIdx.x == 0) {
-        for (int64_t j = p.T; j < SDS_MAX_CHUNK_FRAMES; ++j)
-          st->pub.motion_d[j] = __longlong_as_double(0x7FF8000000000000ll);
-        if (st->mot_count > 0) {
-          double mx = 0.0;
-          for (int64_t q = 0; q < st->mot_count; ++q) mx = fmax(mx, st->mot_window[q]);
-          const double dhat = fmin(1.0, mx / p.sigma);
-          const double target = p.s_min + (p.s_max - p.s_min) * dhat;
-          st->pub.noise_rate = st->pub.noise_rate + (1.0 - p.lam) * (target - st->pub.noise_rate);
-          st->pub.motion_dhat = dhat;
-        }
-        st->mot_has_prev = 1;
-      }
+      if (j < SDS_MAX_CHUNK_FRAMES) st->pub.motion_d[j] = dv;
     }
+    for (int64_t j = p.T; j < SDS_MAX_CHUNK_FRAMES; ++j) st->pub.motion_d[j] = nan;
+    double new_rate = rate, dhat = dhat_old;
+    if (count > 0) {
+      double mx = 0.0;
+      for (int64_t q = 0; q < count; ++q) mx = fmax(mx, st->mot_window[q]);
+      dhat = fmin(1.0, mx / p.sigma);
+      const double target = p.s_min + (p.s_max - p.s_min) * dhat;
+      new_rate = rate + (1.0 - p.lam) * (target - rate);
+    }
+    st->mot_head = head;
+    st->mot_count = count;
+    st->pub.motion_pairs = pairs;
+    st->pub.noise_rate = new_rate;
+    st->pub.motion_dhat = dhat;
+    st->mot_has_prev = 1;
   }
 }
 
-__global__ void __launch_bounds__(kStepThreads) step_kernel(const StepParams p) {
-  __shared__ double red[kWarps];
+// Run by the last block: every sum of the launch is reduced by one warp in
+// a fixed order (lane-strided over the partials, then a butterfly, which
+// leaves the same bits in every lane), and one thread per stream takes the
+// stream's decisions.  The three SSF sums of a stream follow one order, so
+// identical frames still give dot == |I|^2 == |R|^2 bitwise.
+__device__ void finalize(const StepParams& p, double* fin) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_ssf = p.ssf_frame ? 3 : 0;
+  const int per_s = n_ssf + (p.mot_chunk ? (int)p.T : 0);
+  for (int64_t s0 = 0; s0 < p.S; s0 += kFinChunk) {
+    const int ns = (int)min((int64_t)kFinChunk, p.S - s0);
+    for (int k = warp; k < ns * per_s; k += kWarps) {
+      const int64_t s = s0 + k / per_s;
+      const int q = k % per_s;
+      const double* base;
+      int64_t n, stride;
+      if (q < n_ssf) {
+        base = p.partials + s * p.nb_s * 3 + q;
+        n = p.nb_s;
+        stride = 3;
+      } else {
+        base = p.partials + p.S * p.nb_s * 3 + (s * p.T + (q - n_ssf)) * p.nb_m;
+        n = p.nb_m;
+        stride = 1;
+      }
+      double v = 0.0;
+      for (int64_t i = lane; i < n; i += 32) v += __ldcg(base + i * stride);
+      v = warp_sum(v);
+      if (lane == 0) fin[k] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < ns; i += kStepThreads) decide(p, s0 + i, fin + i * per_s);
+    __syncthreads();
+  }
+}
+
+template <int N>
+__global__ void __launch_bounds__(kStepThreads, 2) step_kernel(const StepParams p) {
+  __shared__ dfloat red[3 * kWarps];
+  __shared__ double fin[kFinChunk * kFinPer];
   __shared__ int is_last;
   const int64_t tot_u = p.n > 0 ? p.S * p.nb_u : 0;
   const int64_t tot_s = p.ssf_frame ? p.S * p.nb_s : 0;
   const int64_t tot_m = p.mot_chunk ? p.S * p.T * p.nb_m : 0;
-  const int64_t total = tot_u + tot_s + tot_m;
+  const int64_t tot_r = tot_s + tot_m;  // reduction units come first
+  const int64_t total = tot_u + tot_r;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-    if (w < tot_u) {
-      update_block(p, w);
-    } else if (w < tot_u + tot_s) {
-      ssf_block(p, w - tot_u, red);
+    if (w < tot_r) {
+      if (w < tot_s) {
+        ssf_block(p, w, red);
+      } else {
+        motion_block(p, w - tot_s, red);
+      }
+      // Count the finished reduction unit (thread 0 wrote its partials);
+      // the unit that completes the set finishes the launch's decisions
+      // while other blocks go on streaming the update.
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned int prev = atomicAdd(p.counter, 1u);
+        is_last = (prev == (unsigned int)(tot_r - 1)) ? 1 : 0;
+      }
+      __syncthreads();
+      if (is_last) {
+        __threadfence();
+        finalize(p, fin);
+        if (threadIdx.x == 0) {
+          *p.counter = 0u;
+          __threadfence();
+        }
+      }
     } else {
-      motion_block(p, w - tot_u - tot_s, red);
+      update_block<N>(p, w - tot_r);
     }
-  }
-  if (tot_s + tot_m == 0) return;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int prev = atomicAdd(p.counter, 1u);
-    is_last = (prev == gridDim.x - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  finalize(p, red);
-  if (threadIdx.x == 0) {
-    *p.counter = 0u;
-    __threadfence();
   }
 }
 
@@ -260,7 +370,18 @@ cudaError_t launch_step(const StepParams& p, int sm_count, cudaStream_t st) {
   if (tot == 0) return cudaSuccess;
   const int64_t cap = (int64_t)sm_count * (2048 / kStepThreads);
   const int grid = (int)(tot < cap ? tot : cap);
-  step_kernel<<<grid, kStepThreads, 0, st>>>(p);
+  switch (p.n) {
+    case 0:
+    case 1: step_kernel<1><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 2: step_kernel<2><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 3: step_kernel<3><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 4: step_kernel<4><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 5: step_kernel<5><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 6: step_kernel<6><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 7: step_kernel<7><<<grid, kStepThreads, 0, st>>>(p); break;
+    case 8: step_kernel<8><<<grid, kStepThreads, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -46,4 +46,21 @@ __device__ __forceinline__ uint4 rope8(uint4 v, int e0, const int pos[3], const 
   return v;
 }
 
+// Rotate 8 consecutive elements (4 pairs) with the pairs' (cos, sin) given.
+__device__ __forceinline__ uint32_t rope_pair_cs(uint32_t w, float2 cs) {
+  const float u = bf16_lo(w), v = bf16_hi(w);
+  const float r0 = __fmaf_rn(u, cs.x, -v * cs.y);
+  const float r1 = __fmaf_rn(u, cs.y, v * cs.x);
+  __nv_bfloat162 out = __floats2bfloat162_rn(r0, r1);
+  return *reinterpret_cast<uint32_t*>(&out);
+}
+
+__device__ __forceinline__ uint4 rope8_cs(uint4 v, const float2 (&cs)[4]) {
+  v.x = rope_pair_cs(v.x, cs[0]);
+  v.y = rope_pair_cs(v.y, cs[1]);
+  v.z = rope_pair_cs(v.z, cs[2]);
+  v.w = rope_pair_cs(v.w, cs[3]);
+  return v;
+}
+
 }  // namespace sds

@@ -212,9 +212,9 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
       tab_entries += (int64_t)rows[a] * (seg[a] / 2);
     }
   }
-  const int64_t nb_u = cdiv(c.slot_elems, kStepBlockElems);
-  const int64_t nb_s = c.ssf_on ? cdiv(c.ssf_elems, kStepBlockElems) : 0;
-  const int64_t nb_m = c.motion_on ? cdiv(c.frame_elems, kStepBlockElems) : 0;
+  const int64_t nb_u = cdiv(c.slot_elems, kUpdBlockElems);
+  const int64_t nb_s = c.ssf_on ? cdiv(c.ssf_elems, kRedBlockElems) : 0;
+  const int64_t nb_m = c.motion_on ? cdiv(c.frame_elems, kRedBlockElems) : 0;
   const int64_t ssf_ref = c.ssf_on ? 2 * S * c.ssf_elems : 0;
   const int64_t mot_prev = c.motion_on ? 2 * S * c.frame_elems : 0;
   const int64_t partials = S * nb_s * 3 + S * c.frames_T * nb_m;

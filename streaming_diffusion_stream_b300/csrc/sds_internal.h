@@ -144,7 +144,8 @@ struct StepParams {
 void set_thread_error(const char* msg);
 
 constexpr int kStepThreads = 256;
-constexpr int kStepBlockElems = 2048;  // elements per work block (8 per thread)
+constexpr int kRedBlockElems = 8192;  // elements per SSF / motion work block (32 per thread)
+constexpr int kUpdBlockElems = 1024;  // elements per update work block (4 per thread)
 cudaError_t launch_step(const StepParams& p, int sm_count, cudaStream_t st);
 
 }  // namespace sds
