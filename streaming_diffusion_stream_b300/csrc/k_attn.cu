@@ -58,7 +58,7 @@ namespace {
 constexpr int BM = 128;         // query rows per tile (two tiles per item)
 constexpr int BN = 128;         // keys per tile
 constexpr int SUB = 128 * 128;  // bytes of one 128-row x 64-column bf16 sub-tile
-constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA issuer
+constexpr int kThreads = 352;   // 8 softmax warps + producer + 2 MMA issuers
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
@@ -70,7 +70,14 @@ struct Cfg {
   // d = 64 leaves 64 spare tensor-memory columns after each O accumulator:
   // P goes there, S stays intact, and exponentials are taken speculatively
   // against the running max (a tile that raises it is redone from S).
-  static constexpr bool SPEC = (D == 64);
+  static constexpr bool SPEC = false;
+  // d = 64: an M128 N64 MMA from one issuing thread takes about 50 cycles
+  // against 32 of tensor work, while two threads issuing concurrently reach
+  // the full rate.  So each group's P V product is split: kk-steps 0,2,4,6
+  // by issuer A into O columns [0,64), 1,3,5,7 by issuer B into [64,128);
+  // the epilogue adds the halves.
+  static constexpr bool DUAL = (D == 64);
+  static constexpr int OCOLS = DUAL ? 128 : D;  // tensor-memory columns of one O
   static constexpr int Q = 0;
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
@@ -101,7 +108,8 @@ struct Bars {
   uint64_t* s_full;  // [2]
   uint64_t* p_full;  // [2]
   uint64_t* o_done;  // [2]
-  uint64_t* mma_final;
+  uint64_t* mma_final;  // [2]: issuer A, issuer B
+  uint64_t* pvb_done;   // [2]: issuer B's half of PV_t has landed
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -122,7 +130,8 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.p_full = r.s_full + 2;
   r.o_done = r.p_full + 2;
   r.mma_final = r.o_done + 2;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(r.mma_final + 1);
+  r.pvb_done = r.mma_final + 2;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.pvb_done + 2);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   return r;
 }
@@ -232,14 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B.k_full + i, 1);
       mbar_init(B.v_full + i, 1);
       mbar_init(B.k_empty + i, 1);
-      mbar_init(B.v_empty + i, 1);
+      mbar_init(B.v_empty + i, C::DUAL ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.s_full + i, 1);
       mbar_init(B.p_full + i, 128);
-      mbar_init(B.o_done + i, 1);
+      mbar_init(B.o_done + i, C::DUAL ? 2 : 1);
+      mbar_init(B.pvb_done + i, 1);
+      mbar_init(B.mma_final + i, 1);
     }
-    mbar_init(B.mma_final, 1);
     *B.abort_flag = 0;
     fence_barrier_init();
   }
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aP = C::SPEC ? dO + 64u : tmem + (uint32_t)(t * 128);
         const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
+        for (int kk = 0; kk < BN / 16; kk += (C::DUAL ? 2 : 1))
           mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4), dhi,
                         IDESC_O, (acc || kk > 0) ? 1u : 0u);
       };
@@ -388,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 0);
           const int qb1 = boundary ? qb_n : sg % C::QB;
           if (more) {
-            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n)) {
+            // S0(g+1) overwrites P0(g): issuer B's half of PV0(g) must have read it
+            if ((C::DUAL && !mbar_wait(B.pvb_done + 0, g & 1u)) ||
+                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n))) {
               ok = false;
               break;
             }
@@ -405,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 1);
           mma_commit(B.v_empty + st);
           if (more) {
-            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n)) {
+            if ((C::DUAL && !mbar_wait(B.pvb_done + 1, g & 1u)) ||
+                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n))) {
               ok = false;
               break;
             }
@@ -421,10 +434,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) fail_wait(B);
       // all our MMAs complete before tensor memory is released
-      mma_commit(B.mma_final);
-      mbar_wait(B.mma_final, 0);
+      mma_commit(B.mma_final + 0);
+      mbar_wait(B.mma_final + 0, 0);
     }
-  } else if (active) {
+  } else if (wid == 10) {
+    // ------------------------------------------------------------ MMA issuer B (d = 64):
+    // the odd kk-steps of every P V product, into the second half of O
+    if (C::DUAL && lane == 0 && active) {
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
+      const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
+      const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
+      bool ok = true;
+      uint32_t g = 0;
+      int64_t u = u_lo;
+      while (ok && u < u_hi) {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        const int n_here = (int)(seg_hi - u);
+        for (int i = 0; i < n_here; ++i, ++g) {
+          const uint32_t st = g % C::ST, ph = (g / C::ST) & 1u;
+          if (!mbar_wait(B.v_full + st, ph)) {
+            ok = false;
+            break;
+          }
+          const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait(B.p_full + t, g & 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dO = tmem + 256u + (uint32_t)(t * 128) + 64u;
+            const uint32_t aP = tmem + (uint32_t)(t * 128);
+#pragma unroll
+            for (int kk = 1; kk < BN / 16; kk += 2)
+              mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4),
+                            dhi, IDESC_O, (i > 0 || kk > 1) ? 1u : 0u);
+            mma_commit(B.o_done + t);
+            mma_commit(B.pvb_done + t);
+          }
+          if (!ok) break;
+          mma_commit(B.v_empty + st);
+        }
+        u = seg_hi;
+      }
+      if (!ok) fail_wait(B);
+      mma_commit(B.mma_final + 1);
+      mbar_wait(B.mma_final + 1, 0);
+    }
+  } else if (wid < 8 && active) {
     // ------------------------------------------------------------ softmax groups
     const int t = wid >> 2;   // query tile of this group
     const int r = tid & 127;  // row within the tile == TMEM lane
@@ -432,6 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_base;
     const uint32_t tO = tmem + 256u + (uint32_t)(t * 128) + lane_base;
     const uint32_t tP = C::SPEC ? tO + 64u : tS;  // packed bf16 probabilities
+    // 32 columns of this row's O (the sum of the two halves for d = 64)
+    auto load_o = [&](int c, float(&tmp)[32]) {
+      tmem_ld32(tO + (uint32_t)(c * 32), tmp);
+      if (C::DUAL) {
+        float t2[32];
+        tmem_ld32(tO + 64u + (uint32_t)(c * 32), t2);
+        tmem_wait_ld();
+        reg_fence32(tmp);
+        reg_fence32(t2);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) tmp[q] += t2[q];
+      } else {
+        tmem_wait_ld();
+        reg_fence32(tmp);
+      }
+    };
     const float sc = p.scale_log2;
     const float2 sc2 = make_float2(sc, sc);
     int64_t u = u_lo;
@@ -574,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < C::OCOLS / 32; ++c) {
             float tmp[32];
             tmem_ld32(tO + (uint32_t)(c * 32), tmp);
             tmem_wait_ld();
@@ -606,9 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float tmp[32];
-          tmem_ld32(tO + (uint32_t)(c * 32), tmp);
-          tmem_wait_ld();
-          reg_fence32(tmp);
+          load_o(c, tmp);
           if (row < p.q_rows) {
 #pragma unroll
             for (int q = 0; q < 32; q += 8) {
@@ -629,9 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float tmp[32];
-          tmem_ld32(tO + (uint32_t)(c * 32), tmp);
-          tmem_wait_ld();
-          reg_fence32(tmp);
+          load_o(c, tmp);
 #pragma unroll
           for (int q = 0; q < 32; q += 4)
             __stcg(reinterpret_cast<float4*>(wo + c * 32 + q),
