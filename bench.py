@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--streams", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep-streams", type=int, default=0,
+                    help="print one line per stream count B = 1..N (same workload, one GPU)")
     return ap.parse_args()
 
 
@@ -560,10 +562,45 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Frames/s of the step for B = 1..N concurrent streams in one context:
+    the throughput curve whose flattening is the roofline knee."""
+    import torch
+    torch.cuda.set_device(0)
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    rows = []
+    for b in range(1, args.sweep_streams + 1):
+        w = W.get_config(args.workload, streams=b)
+        run = Runner(w, pool_bytes_min=2.0 * l2)
+        for i in range(max(3, args.warmup)):
+            run.step(run.sets[i % run.n_sets])
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(args.steps):
+            run.step(run.sets[i % run.n_sets])
+        e.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(e) / args.steps
+        run.close()
+        fps = frames_per_step(w) / (ms / 1e3)
+        rows.append({"streams": b, "ms_per_step": round(ms, 4), "frames_per_s": round(fps, 1),
+                     "per_stream_frames_per_s": round(fps / b, 1),
+                     "attn_tflops": round(attn_flops(w) / (ms / 1e3) / 1e12, 1)})
+        print(json.dumps({"sweep": args.workload, **rows[-1]}), flush=True)
+    gains = [rows[i]["frames_per_s"] / rows[i - 1]["frames_per_s"] for i in range(1, len(rows))]
+    knee = next((rows[i]["streams"] for i, g in enumerate(gains) if g < 1.05), rows[-1]["streams"])
+    print(json.dumps({"sweep_summary": args.workload, "knee_streams": knee,
+                      "frames_per_s": [r["frames_per_s"] for r in rows]}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep_streams:
+        run_sweep(args)
     else:
         run_ours(args)
 

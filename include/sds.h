@@ -350,6 +350,67 @@ SDS_API sds_status sds_ssf_noalloc(const float* frame, const float* ref, const f
                                    int64_t max_skip, double* cos_out, double* p_out,
                                    int64_t* skip_out, sds_stream_t stream);
 
+/*
+ * Checkpoints.  A checkpoint is an sds_state_header followed by a payload of
+ * 8-byte aligned sections, in this order:
+ *   meta      int64[8]: frames pushed F, RoPE offset o, last chunk start p0,
+ *             first frame of the last chunk, sinks filled, RoPE resets,
+ *             chunks pushed, motion updates done
+ *   records   S per-stream device records (devstate_bytes each; the public
+ *             sds_stream_state first, then private SSF / motion fields)
+ *   sink_emb  fp32 [S][M][D]
+ *   ssf_ref   fp32 [2][S][ssf_elems]      (when ssf_on)
+ *   mot_prev  fp32 [2][S][frame_elems]    (when motion_on)
+ *   kv_k, kv_v bf16 [S][(M+R)*L][H][d]    (when flags bit 0: with K/V)
+ * payload_hash and config_hash are 64-bit FNV-1a hashes of the payload bytes
+ * and of the sds_config bytes.  A checkpoint restores only into a context
+ * created with a byte-identical sds_config.
+ */
+#define SDS_STATE_MAGIC "SDSSTAT1"
+#define SDS_STATE_RECORD_BYTES 720 /* devstate_bytes of this ABI version */
+typedef struct {
+  char magic[8];           /* SDS_STATE_MAGIC without its terminating NUL */
+  int64_t abi_version;     /* SDS_ABI_VERSION of the writer */
+  uint64_t config_hash;
+  int64_t flags;           /* bit 0: K/V ring and sinks included */
+  int64_t payload_bytes;
+  uint64_t payload_hash;
+  int64_t streams;
+  int64_t devstate_bytes;  /* size of one per-stream device record */
+  int64_t emb_elems, ssf_ref_elems, mot_prev_elems, kv_elems; /* per tensor */
+  int64_t reserved[4];     /* zero */
+} sds_state_header;
+
+/*
+ * Write a checkpoint of ctx to buf (host memory, *len bytes available).
+ * with_kv != 0 includes the K/V ring and sinks (the bulk of the bytes).
+ * buf == NULL: only stores the needed size in *len.  Synchronises `stream`
+ * first, so the checkpoint reflects all work enqueued before the call.
+ * Errors: SDS_ERR_INVALID_ARG (len NULL, or *len too small: *len then holds
+ * the needed size), SDS_ERR_CUDA.
+ */
+SDS_API sds_status sds_state_export(sds_ctx* ctx, void* buf, size_t* len, int64_t with_kv,
+                                    sds_stream_t stream);
+
+/*
+ * Restore a checkpoint written by sds_state_export into ctx.  The buffer is
+ * validated first (sds_state_check against ctx's config); a rejected buffer
+ * changes nothing.  A checkpoint without K/V leaves the ring and sinks as
+ * they are.  Synchronises `stream` before returning (buf may be freed then).
+ * Errors: SDS_ERR_STATE (bad magic, version, config, sizes or payload hash),
+ * SDS_ERR_CUDA (the copy failed: destroy the context).
+ */
+SDS_API sds_status sds_state_import(sds_ctx* ctx, const void* buf, size_t len,
+                                    sds_stream_t stream);
+
+/*
+ * Validate a checkpoint against a configuration without touching any
+ * device: magic, ABI version, config hash, section sizes and payload hash.
+ * Returns SDS_OK or SDS_ERR_STATE / SDS_ERR_INVALID_ARG with a message in
+ * sds_last_error(NULL).
+ */
+SDS_API sds_status sds_state_check(const sds_config* cfg, const void* buf, size_t len);
+
 /* Synchronise `stream` and copy the S per-stream decision records to host
  * memory out[0..S-1]. */
 SDS_API sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream);

@@ -64,6 +64,9 @@ def lib():
         L.orc_step_update.argtypes = [P] * 9
         L.orc_ssf.argtypes = [P, P, C.c_float, P, P]
         L.orc_motion.argtypes = [P, P, P]
+        L.orc_set_lazy.argtypes = [P, C.c_int]
+        L.orc_provenance.argtypes = [P, P]
+        L.orc_materialize.argtypes = [P, P, P]
         L.orc_noise_rate.restype = _f64
         L.orc_noise_rate.argtypes = [P]
         L.orc_skip_count.restype = _i64
@@ -260,3 +263,21 @@ class Stream:
 
     def noise_rate(self) -> float:
         return float(lib().orc_noise_rate(self.h))
+
+    def set_lazy(self, on: bool = True) -> None:
+        """Pushes record provenance only; K/V are built later by materialize()."""
+        lib().orc_set_lazy(self.h, int(on))
+
+    def provenance(self) -> np.ndarray:
+        """[M+R][3]: (chunk index, frame in chunk, chunk start p0) per key frame, -1 if unwritten."""
+        w = self.w
+        out = np.zeros((w["M"] + w["R"], 3), dtype=np.int64)
+        lib().orc_provenance(self.h, _p(out))
+        return out
+
+    def materialize(self, k_frames: np.ndarray, v_frames: np.ndarray) -> None:
+        """Write every key frame with a provenance from the raw frames given in
+        buffer order ([M+R][L][H][d] bf16), exactly as push writes them."""
+        k = np.ascontiguousarray(k_frames, dtype=np.uint16)
+        v = np.ascontiguousarray(v_frames, dtype=np.uint16)
+        lib().orc_materialize(self.h, _p(k), _p(v))

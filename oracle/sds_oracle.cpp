@@ -200,6 +200,10 @@ struct Stream {
   int has_prev = 0;
   std::vector<double> window;
   double s_rate = 0.0;
+  // lazy mode: pushes record where each key frame came from instead of
+  // rotating it; materialize later applies the push arithmetic to the frames
+  int lazy = 0;
+  std::vector<long long> prov;  // [M+R][3]: source chunk index, frame in chunk, chunk start p0
 };
 
 long long key_frames(const orc_cfg& c) { return c.image_mode ? 0 : (c.M + c.R); }
@@ -281,6 +285,7 @@ void* orc_create(const orc_cfg* c) {
   s->ref.assign((size_t)c->ssf_E, 0.0f);
   s->prev.assign((size_t)c->N_f, 0.0f);
   s->s_rate = c->s_min;
+  s->prov.assign((size_t)(key_frames(*c) * 3), -1);
   return s;
 }
 
@@ -290,6 +295,32 @@ void orc_destroy(void* p) { delete (Stream*)p; }
 // oldest frame by overwrite).  k, v: bf16 [T*L][H][d].  Returns p0.
 // reading: "frame index exceeds tau" compares the chunk's start position,
 // counted from the last reset, with tau; cached keys keep their rotation.
+// One frame of a pushed chunk into key frame `dst_frame` of the buffer:
+// each key vector rotated at (pos_t, y, x) in double and rounded to bf16,
+// the values copied.  kf, vf: bf16 [L][H][d] of the frame.
+static void write_frame(Stream* s, long long dst_frame, const uint16_t* kf, const uint16_t* vf,
+                        long long pos_t) {
+  const orc_cfg& c = s->c;
+  long long HD = c.H * c.d;
+  std::vector<double> in((size_t)c.d), out((size_t)c.d);
+  for (long long l = 0; l < c.L; ++l) {
+    size_t src = (size_t)(l * HD);
+    size_t dst = (size_t)((dst_frame * c.L + l) * HD);
+    long long pos[3] = {pos_t, l / c.grid_w, l % c.grid_w};
+    for (long long h = 0; h < c.H; ++h) {
+      const uint16_t* kr = kf + src + h * c.d;
+      if (c.rope_on) {
+        for (long long t = 0; t < c.d; ++t) in[(size_t)t] = bf16_to_double(kr[t]);
+        rope_rotate(in.data(), out.data(), c.d, pos, c.rope_base);
+        for (long long t = 0; t < c.d; ++t) s->kbuf[dst + h * c.d + t] = double_to_bf16(out[(size_t)t]);
+      } else {
+        std::memcpy(&s->kbuf[dst + h * c.d], kr, (size_t)c.d * 2);
+      }
+    }
+    std::memcpy(&s->vbuf[dst], vf + src, (size_t)HD * 2);
+  }
+}
+
 long long orc_push(void* p, const uint16_t* k, const uint16_t* v) {
   Stream* s = (Stream*)p;
   const orc_cfg& c = s->c;
@@ -300,32 +331,46 @@ long long orc_push(void* p, const uint16_t* k, const uint16_t* v) {
     s->resets++;
   }
   s->p0 = p0;
-  long long HD = c.H * c.d;
-  std::vector<double> in((size_t)c.d), out((size_t)c.d);
+  const size_t fr = (size_t)(c.L * c.H * c.d);
   for (long long j = 0; j < c.T; ++j) {
     long long f = s->F + j;
     long long slot = f % c.R;
-    for (long long l = 0; l < c.L; ++l) {
-      size_t src = (size_t)((j * c.L + l) * HD);
-      size_t dst = (size_t)(((c.M + slot) * c.L + l) * HD);
-      long long pos[3] = {p0 + j, l / c.grid_w, l % c.grid_w};
-      for (long long h = 0; h < c.H; ++h) {
-        const uint16_t* kr = k + src + h * c.d;
-        if (c.rope_on) {
-          for (long long t = 0; t < c.d; ++t) in[(size_t)t] = bf16_to_double(kr[t]);
-          rope_rotate(in.data(), out.data(), c.d, pos, c.rope_base);
-          for (long long t = 0; t < c.d; ++t) s->kbuf[dst + h * c.d + t] = double_to_bf16(out[(size_t)t]);
-        } else {
-          std::memcpy(&s->kbuf[dst + h * c.d], kr, (size_t)c.d * 2);
-        }
-      }
-      std::memcpy(&s->vbuf[dst], v + src, (size_t)HD * 2);
-    }
+    long long* pv = &s->prov[(size_t)((c.M + slot) * 3)];
+    pv[0] = s->pushes;
+    pv[1] = j;
+    pv[2] = p0;
+    if (!s->lazy) write_frame(s, c.M + slot, k + j * fr, v + j * fr, p0 + j);
   }
   s->chunk_first = s->F;
   s->F += c.T;
   s->pushes++;
   return p0;
+}
+
+// Lazy mode on/off (see Stream::prov).  Only for a stream that has not
+// pushed yet.
+void orc_set_lazy(void* p, int on) { ((Stream*)p)->lazy = on; }
+
+// Provenance of every key frame: [M+R][3] = (chunk index, frame in chunk,
+// chunk start position p0), -1 for a frame never written.
+void orc_provenance(void* p, long long* out) {
+  Stream* s = (Stream*)p;
+  std::memcpy(out, s->prov.data(), s->prov.size() * sizeof(long long));
+}
+
+// Fill the K/V buffer from raw (unrotated) frames given for every key frame
+// in buffer order, kf, vf: bf16 [M+R][L][H][d]; each frame with a provenance
+// is written as its push wrote it (rotated at p0 + frame in chunk).
+void orc_materialize(void* p, const uint16_t* kf, const uint16_t* vf) {
+  Stream* s = (Stream*)p;
+  const orc_cfg& c = s->c;
+  const size_t fr = (size_t)(c.L * c.H * c.d);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long f = 0; f < key_frames(c); ++f) {
+    const long long* pv = &s->prov[(size_t)(f * 3)];
+    if (pv[0] < 0) continue;
+    write_frame(s, f, kf + (size_t)f * fr, vf + (size_t)f * fr, pv[2] + pv[1]);
+  }
 }
 
 // meta: F, o, p0, ring valid frames, sinks filled, resets
@@ -343,6 +388,8 @@ static void copy_frame_to_sink(Stream* s, long long sink, long long chunk_frame)
   const orc_cfg& c = s->c;
   long long slot = (s->chunk_first + chunk_frame) % c.R;
   size_t fr = (size_t)(c.L * c.H * c.d);
+  for (int q = 0; q < 3; ++q) s->prov[(size_t)(sink * 3 + q)] = s->prov[(size_t)((c.M + slot) * 3 + q)];
+  if (s->lazy) return;
   std::memcpy(&s->kbuf[(size_t)sink * fr], &s->kbuf[(size_t)(c.M + slot) * fr], fr * 2);
   std::memcpy(&s->vbuf[(size_t)sink * fr], &s->vbuf[(size_t)(c.M + slot) * fr], fr * 2);
 }

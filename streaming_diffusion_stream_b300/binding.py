@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libsds.so")
 SDS_ABI_VERSION = 2
 SDS_MAX_SLOTS = 8
 SDS_MAX_CHUNK_FRAMES = 8
+SDS_STATE_MAGIC = b"SDSSTAT1"
+SDS_STATE_RECORD_BYTES = 720
 
 SDS_OK, SDS_ERR_INVALID_ARG, SDS_ERR_OOM, SDS_ERR_CUDA, SDS_ERR_STATE, SDS_ERR_UNSUPPORTED = range(6)
 STATUS_NAMES = {0: "SDS_OK", 1: "SDS_ERR_INVALID_ARG", 2: "SDS_ERR_OOM", 3: "SDS_ERR_CUDA",
@@ -67,6 +69,14 @@ class sds_buffers(C.Structure):
     _fields_ = [("kv_k", _P), ("kv_v", _P), ("sink_emb", _P), ("kv_rows", _i64)]
 
 
+class sds_state_header(C.Structure):
+    _fields_ = [("magic", C.c_char * 8), ("abi_version", _i64), ("config_hash", C.c_uint64),
+                ("flags", _i64), ("payload_bytes", _i64), ("payload_hash", C.c_uint64),
+                ("streams", _i64), ("devstate_bytes", _i64), ("emb_elems", _i64),
+                ("ssf_ref_elems", _i64), ("mot_prev_elems", _i64), ("kv_elems", _i64),
+                ("reserved", _i64 * 4)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "sds_abi_version": (C.c_int, []),
@@ -83,6 +93,9 @@ SIGNATURES = {
     "sds_read_state": (C.c_int, [_P, C.POINTER(sds_stream_state), _P]),
     "sds_get_meta": (C.c_int, [_P, C.POINTER(sds_meta)]),
     "sds_get_buffers": (C.c_int, [_P, C.POINTER(sds_buffers)]),
+    "sds_state_export": (C.c_int, [_P, _P, C.POINTER(C.c_size_t), _i64, _P]),
+    "sds_state_import": (C.c_int, [_P, _P, C.c_size_t, _P]),
+    "sds_state_check": (C.c_int, [C.POINTER(sds_config), _P, C.c_size_t]),
 }
 
 _lib = None
@@ -247,3 +260,21 @@ def sds_get_buffers(ctx) -> dict:
     b = sds_buffers()
     check(lib().sds_get_buffers(ctx, C.byref(b)), ctx)
     return {n: getattr(b, n) for n, _ in b._fields_}
+
+
+def sds_state_export(ctx, with_kv: bool = True, stream=None) -> bytes:
+    """Checkpoint of the context (synchronises `stream`) as bytes."""
+    n = C.c_size_t(0)
+    check(lib().sds_state_export(ctx, None, C.byref(n), int(with_kv), _stream(stream)), ctx)
+    buf = C.create_string_buffer(n.value)
+    check(lib().sds_state_export(ctx, buf, C.byref(n), int(with_kv), _stream(stream)), ctx)
+    return buf.raw[:n.value]
+
+
+def sds_state_import(ctx, data: bytes, stream=None) -> None:
+    check(lib().sds_state_import(ctx, data, len(data), _stream(stream)), ctx)
+
+
+def sds_state_check(cfg: sds_config, data: bytes) -> None:
+    """Validate a checkpoint against a configuration (no device access)."""
+    check(lib().sds_state_check(C.byref(cfg), data, len(data)))

@@ -177,7 +177,6 @@ struct SegIter {
   }
   __device__ __forceinline__ bool done() const { return u >= u_hi; }
   __device__ __forceinline__ bool first() const { return u == seg_lo; }
-  __device__ __forceinline__ bool last() const { return u + 1 == seg_hi; }
   __device__ __forceinline__ int kt() const { return (int)(u - item * nkt); }
   __device__ __forceinline__ void advance() {
     ++u;

@@ -171,6 +171,95 @@ void fill_attn_rope(const sds_ctx* c, AttnParams& ap) {
   ap.rope_tab = c->rope_tab;
 }
 
+// ----------------------------------------------------------------- checkpoints
+
+uint64_t fnv1a(const void* data, size_t n, uint64_t h = 14695981039346656037ull) {
+  const unsigned char* b = static_cast<const unsigned char*>(data);
+  for (size_t i = 0; i < n; ++i) {
+    h ^= b[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+// Section sizes (bytes) of a checkpoint payload for a configuration.
+struct StateLayout {
+  int64_t meta, records, emb, ssf, mot, kv;  // kv: per tensor (K and V each)
+  int64_t emb_elems, ssf_elems, mot_elems, kv_elems;
+  bool with_kv;
+  int64_t payload() const { return meta + records + emb + ssf + mot + (with_kv ? 2 * kv : 0); }
+};
+
+StateLayout state_layout(const sds_config& c, bool with_kv) {
+  StateLayout L{};
+  const bool image = c.ring_R == 0;
+  const int64_t S = c.streams;
+  L.with_kv = with_kv;
+  L.emb_elems = image ? 0 : S * c.sink_M * (c.emb_dim_D > 0 ? c.emb_dim_D : 0);
+  L.ssf_elems = c.ssf_on ? 2 * S * c.ssf_elems : 0;
+  L.mot_elems = c.motion_on ? 2 * S * c.frame_elems : 0;
+  L.kv_elems = image ? 0 : S * (c.sink_M + c.ring_R) * c.tokens_L * c.heads_H * c.head_dim;
+  L.meta = 8 * 8;
+  L.records = S * (int64_t)sizeof(DevState);
+  L.emb = L.emb_elems * 4;
+  L.ssf = L.ssf_elems * 4;
+  L.mot = L.mot_elems * 4;
+  L.kv = L.kv_elems * 2;
+  return L;
+}
+
+// Validate a checkpoint against a configuration; on failure `why` says why.
+sds_status check_state(const sds_config& c, const void* buf, size_t len, std::string& why) {
+  if (!buf) {
+    why = "checkpoint buffer is NULL";
+    return SDS_ERR_INVALID_ARG;
+  }
+  if (len < sizeof(sds_state_header)) {
+    why = "checkpoint shorter than its header";
+    return SDS_ERR_STATE;
+  }
+  sds_state_header h;
+  std::memcpy(&h, buf, sizeof h);
+  if (std::memcmp(h.magic, SDS_STATE_MAGIC, 8) != 0) {
+    why = "not a checkpoint (bad magic)";
+    return SDS_ERR_STATE;
+  }
+  if (h.abi_version != SDS_ABI_VERSION) {
+    why = "checkpoint written by another ABI version";
+    return SDS_ERR_STATE;
+  }
+  if (h.config_hash != fnv1a(&c, sizeof c)) {
+    why = "checkpoint belongs to a different configuration";
+    return SDS_ERR_STATE;
+  }
+  const StateLayout L = state_layout(c, (h.flags & 1) != 0);
+  if ((h.flags & ~int64_t(1)) != 0 || h.streams != c.streams ||
+      h.devstate_bytes != (int64_t)sizeof(DevState) || h.emb_elems != L.emb_elems ||
+      h.ssf_ref_elems != L.ssf_elems || h.mot_prev_elems != L.mot_elems ||
+      h.kv_elems != L.kv_elems || h.payload_bytes != L.payload()) {
+    why = "checkpoint section sizes do not match the configuration";
+    return SDS_ERR_STATE;
+  }
+  if (len < sizeof h + (size_t)h.payload_bytes) {
+    why = "checkpoint truncated";
+    return SDS_ERR_STATE;
+  }
+  const unsigned char* payload = static_cast<const unsigned char*>(buf) + sizeof h;
+  if (fnv1a(payload, (size_t)h.payload_bytes) != h.payload_hash) {
+    why = "checkpoint payload hash mismatch (corrupted)";
+    return SDS_ERR_STATE;
+  }
+  const int64_t* meta = reinterpret_cast<const int64_t*>(payload);
+  int64_t m[8];
+  std::memcpy(m, meta, sizeof m);
+  if (m[0] < 0 || m[1] < 0 || m[1] > m[0] || m[4] < 0 || m[4] > c.sink_M || m[5] < 0 || m[6] < 0 ||
+      m[7] < 0) {
+    why = "checkpoint metadata out of range";
+    return SDS_ERR_STATE;
+  }
+  return SDS_OK;
+}
+
 }  // namespace
 
 void sds::set_thread_error(const char* msg) { g_create_err = msg; }
@@ -625,6 +714,105 @@ sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds_stream_
   p.ssf_u = u;
   cudaError_t e = launch_step(p, ctx->sm_count, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "ssf launch");
+  return SDS_OK;
+}
+
+sds_status sds_state_check(const sds_config* cfg, const void* buf, size_t len) {
+  if (!cfg) return fail(nullptr, SDS_ERR_INVALID_ARG, "state_check: cfg is NULL");
+  std::string why;
+  const sds_status st = check_state(*cfg, buf, len, why);
+  if (st != SDS_OK) return fail(nullptr, st, "state_check: %s", why.c_str());
+  return SDS_OK;
+}
+
+sds_status sds_state_export(sds_ctx* ctx, void* buf, size_t* len, int64_t with_kv,
+                            sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (!len) return fail(ctx, SDS_ERR_INVALID_ARG, "state_export: len is NULL");
+  const sds_config& c = ctx->cfg;
+  const StateLayout L = state_layout(c, with_kv != 0);
+  const size_t need = sizeof(sds_state_header) + (size_t)L.payload();
+  if (!buf) {
+    *len = need;
+    return SDS_OK;
+  }
+  if (*len < need) {
+    *len = need;
+    return fail(ctx, SDS_ERR_INVALID_ARG, "state_export: buffer of %zu bytes < %zu needed", *len, need);
+  }
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "state_export");
+  unsigned char* out = static_cast<unsigned char*>(buf) + sizeof(sds_state_header);
+  const int64_t meta[8] = {ctx->F, ctx->o, ctx->p0, ctx->chunk_first,
+                           ctx->sinks_filled, ctx->resets, ctx->chunks, ctx->motion_calls};
+  std::memcpy(out, meta, sizeof meta);
+  unsigned char* q = out + L.meta;
+  struct Sec {
+    const void* dev;
+    int64_t bytes;
+  } secs[6] = {{ctx->state, L.records}, {ctx->sink_emb, L.emb}, {ctx->ssf_ref, L.ssf},
+               {ctx->mot_prev, L.mot}, {ctx->kv_k, L.with_kv ? L.kv : 0},
+               {ctx->kv_v, L.with_kv ? L.kv : 0}};
+  for (const Sec& sc : secs) {
+    if (sc.bytes > 0) {
+      e = cudaMemcpy(q, sc.dev, (size_t)sc.bytes, cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "state_export copy");
+    }
+    q += sc.bytes;
+  }
+  sds_state_header h;
+  std::memset(&h, 0, sizeof h);
+  std::memcpy(h.magic, SDS_STATE_MAGIC, 8);
+  h.abi_version = SDS_ABI_VERSION;
+  h.config_hash = fnv1a(&c, sizeof c);
+  h.flags = L.with_kv ? 1 : 0;
+  h.payload_bytes = L.payload();
+  h.payload_hash = fnv1a(out, (size_t)L.payload());
+  h.streams = c.streams;
+  h.devstate_bytes = (int64_t)sizeof(DevState);
+  h.emb_elems = L.emb_elems;
+  h.ssf_ref_elems = L.ssf_elems;
+  h.mot_prev_elems = L.mot_elems;
+  h.kv_elems = L.kv_elems;
+  std::memcpy(buf, &h, sizeof h);
+  *len = need;
+  return SDS_OK;
+}
+
+sds_status sds_state_import(sds_ctx* ctx, const void* buf, size_t len, sds_stream_t stream) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  std::string why;
+  const sds_status st = check_state(ctx->cfg, buf, len, why);
+  if (st != SDS_OK) return fail(ctx, st, "state_import: %s", why.c_str());
+  sds_state_header h;
+  std::memcpy(&h, buf, sizeof h);
+  const StateLayout L = state_layout(ctx->cfg, (h.flags & 1) != 0);
+  const unsigned char* in = static_cast<const unsigned char*>(buf) + sizeof h;
+  int64_t meta[8];
+  std::memcpy(meta, in, sizeof meta);
+  const unsigned char* q = in + L.meta;
+  struct Sec {
+    void* dev;
+    int64_t bytes;
+  } secs[6] = {{ctx->state, L.records}, {ctx->sink_emb, L.emb}, {ctx->ssf_ref, L.ssf},
+               {ctx->mot_prev, L.mot}, {ctx->kv_k, L.with_kv ? L.kv : 0},
+               {ctx->kv_v, L.with_kv ? L.kv : 0}};
+  cudaError_t e = cudaSuccess;
+  for (const Sec& sc : secs) {
+    if (sc.bytes > 0 && e == cudaSuccess)
+      e = cudaMemcpyAsync(sc.dev, q, (size_t)sc.bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    q += sc.bytes;
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "state_import copy");
+  ctx->F = meta[0];
+  ctx->o = meta[1];
+  ctx->p0 = meta[2];
+  ctx->chunk_first = meta[3];
+  ctx->sinks_filled = meta[4];
+  ctx->resets = meta[5];
+  ctx->chunks = meta[6];
+  ctx->motion_calls = meta[7];
   return SDS_OK;
 }
 

@@ -23,6 +23,9 @@ struct DevState {
   double mot_window[kMaxMotionWindow];
 };
 
+static_assert(sizeof(DevState) == SDS_STATE_RECORD_BYTES,
+              "the checkpoint record size is part of the ABI");
+
 // Error bits recorded in DevState::pub.error_word.
 enum : int64_t {
   kErrAttnWaitTimeout = 1 << 0,

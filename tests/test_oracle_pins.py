@@ -502,3 +502,35 @@ def test_motion_clips_at_one_and_window_max():
     assert r["dhat"] == 1.0
     r = s.motion(np.full((1, N), 3.5, dtype=np.float32))   # window {.25, .25}
     assert abs(r["dhat"] - 0.25) < 1e-12
+
+
+def test_lazy_provenance_then_materialize_equals_eager_push():
+    """The long-run checks record provenance and build the ring later; the
+    result must be the ring an eager push sequence builds (through sink
+    fills, refreshes, ring wrap and a RoPE reset)."""
+    w = tiny(M=2, T=3, R=6, rope_tau=5, emb_step=0.8, steps=9)
+    eager, lazy = O.Stream(w), O.Stream(w)
+    lazy.set_lazy(True)
+    walk = W.EmbeddingWalk(w)
+    chunks = []
+    for c in range(9):
+        k, v = W.gen_kv(w, c)
+        chunks.append((k[0], v[0]))
+        eager.push(k[0], v[0])
+        lazy.push(k[0], v[0])
+        h = walk.next()[0]
+        assert eager.sink_refresh(h) == lazy.sink_refresh(h)
+    assert eager.meta() == lazy.meta() and eager.meta()["resets"] >= 1
+    prov = lazy.provenance()
+    TL = w["T"] * w["L"]
+    kf = np.zeros((w["M"] + w["R"], w["L"], w["H"], w["d"]), dtype=np.uint16)
+    vf = np.zeros_like(kf)
+    for f, (c, j, p0) in enumerate(prov):
+        if c >= 0:
+            kf[f] = chunks[c][0].reshape(w["T"], w["L"], w["H"], w["d"])[j]
+            vf[f] = chunks[c][1].reshape(w["T"], w["L"], w["H"], w["d"])[j]
+    lazy.materialize(kf, vf)
+    ke, ve = eager.kv()
+    kl, vl = lazy.kv()
+    assert np.array_equal(ke, kl) and np.array_equal(ve, vl)
+    assert np.array_equal(eager.emb(), lazy.emb())
