@@ -591,8 +591,22 @@ def run_sweep(args):
         print(json.dumps({"sweep": args.workload, **rows[-1]}), flush=True)
     gains = [rows[i]["frames_per_s"] / rows[i - 1]["frames_per_s"] for i in range(1, len(rows))]
     knee = next((rows[i]["streams"] for i, g in enumerate(gains) if g < 1.05), rows[-1]["streams"])
+    # the library's SLO controller fed with the measured step latencies
+    from streaming_diffusion_stream_b300 import binding as B
+    T = frames_per_step(W.get_config(args.workload, streams=1))
+    choices = {}
+    for fps in (30.0, 120.0, 1000.0, 3000.0):
+        ctl = B.SloController(fps, T, 1, args.sweep_streams)
+        for r in rows:
+            ctl.observe(r["streams"], r["ms_per_step"] / 1e3)
+        c = ctl.choose()
+        ctl.close()
+        choices[str(fps)] = {"streams": c["batch"], "meets_slo": c["meets_slo"],
+                             "per_stream_fps": round(c["per_stream_fps"], 1),
+                             "b_slo": c["b_slo"], "b_knee": c["b_knee"]}
     print(json.dumps({"sweep_summary": args.workload, "knee_streams": knee,
-                      "frames_per_s": [r["frames_per_s"] for r in rows]}), flush=True)
+                      "frames_per_s": [r["frames_per_s"] for r in rows],
+                      "slo_controller": choices}), flush=True)
 
 
 def main():

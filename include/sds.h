@@ -411,6 +411,45 @@ SDS_API sds_status sds_state_import(sds_ctx* ctx, const void* buf, size_t len,
  */
 SDS_API sds_status sds_state_check(const sds_config* cfg, const void* buf, size_t len);
 
+/*
+ * SLO-aware stream-batch controller (host only, no device work).
+ * [V2] "SLO-aware batching scheduler": per iteration the system processes
+ * B*T frames (B streams, T frames each) with latency L(T,B); in the
+ * memory-bound regime L is affine in the activation volume, which is linear
+ * in B*T, so the controller fits L = a + b*B*T to the observed latencies
+ * (least squares, older observations down-weighted by `forget`).  A stream
+ * meets the SLO when T / L >= target_fps; the aggregate rate is B*T / L.
+ * The choice is the largest B in [b_min, b_max] that meets the SLO, capped
+ * at the knee: the smallest B whose predicted aggregate rate is within
+ * knee_gain of the rate at b_max (more streams beyond it add latency, not
+ * throughput).  Until two distinct B have been observed it proposes the
+ * next unobserved B from b_min up (exploration).
+ */
+typedef struct sds_slo sds_slo;
+typedef struct {
+  double target_fps;  /* per-stream frame-rate objective, frames/s (> 0) */
+  double forget;      /* weight of an observation after each newer one, (0, 1] */
+  double knee_gain;   /* relative throughput gain below which B stops growing, [0, 1) */
+  int64_t frames_T;   /* frames per stream per iteration (>= 1) */
+  int64_t b_min, b_max; /* 1 <= b_min <= b_max */
+} sds_slo_config;
+
+typedef struct {
+  int64_t batch;          /* chosen B */
+  int64_t meets_slo;      /* 1 if the model predicts T / L(B) >= target_fps */
+  int64_t exploring;      /* 1 while fewer than two distinct B were observed */
+  int64_t b_slo, b_knee;  /* largest B meeting the SLO (0: none), knee B */
+  double a, b;            /* fitted L = a + b*B*T (seconds, seconds per frame) */
+  double latency_s, per_stream_fps, total_fps; /* predicted at the chosen B */
+} sds_slo_choice;
+
+SDS_API sds_status sds_slo_create(const sds_slo_config* cfg, sds_slo** out);
+SDS_API void sds_slo_destroy(sds_slo* c);
+/* Record one iteration: B streams took latency_s seconds (> 0). */
+SDS_API sds_status sds_slo_observe(sds_slo* c, int64_t batch, double latency_s);
+/* The controller's current choice (see above). */
+SDS_API sds_status sds_slo_choose(const sds_slo* c, sds_slo_choice* out);
+
 /* Synchronise `stream` and copy the S per-stream decision records to host
  * memory out[0..S-1]. */
 SDS_API sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream);

@@ -77,6 +77,17 @@ class sds_state_header(C.Structure):
                 ("reserved", _i64 * 4)]
 
 
+class sds_slo_config(C.Structure):
+    _fields_ = [("target_fps", _f64), ("forget", _f64), ("knee_gain", _f64),
+                ("frames_T", _i64), ("b_min", _i64), ("b_max", _i64)]
+
+
+class sds_slo_choice(C.Structure):
+    _fields_ = [("batch", _i64), ("meets_slo", _i64), ("exploring", _i64), ("b_slo", _i64),
+                ("b_knee", _i64), ("a", _f64), ("b", _f64), ("latency_s", _f64),
+                ("per_stream_fps", _f64), ("total_fps", _f64)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "sds_abi_version": (C.c_int, []),
@@ -96,6 +107,10 @@ SIGNATURES = {
     "sds_state_export": (C.c_int, [_P, _P, C.POINTER(C.c_size_t), _i64, _P]),
     "sds_state_import": (C.c_int, [_P, _P, C.c_size_t, _P]),
     "sds_state_check": (C.c_int, [C.POINTER(sds_config), _P, C.c_size_t]),
+    "sds_slo_create": (C.c_int, [C.POINTER(sds_slo_config), C.POINTER(_P)]),
+    "sds_slo_destroy": (None, [_P]),
+    "sds_slo_observe": (C.c_int, [_P, _i64, _f64]),
+    "sds_slo_choose": (C.c_int, [_P, C.POINTER(sds_slo_choice)]),
 }
 
 _lib = None
@@ -278,3 +293,33 @@ def sds_state_import(ctx, data: bytes, stream=None) -> None:
 def sds_state_check(cfg: sds_config, data: bytes) -> None:
     """Validate a checkpoint against a configuration (no device access)."""
     check(lib().sds_state_check(C.byref(cfg), data, len(data)))
+
+
+class SloController:
+    """The library's SLO-aware stream-batch controller (host only)."""
+
+    def __init__(self, target_fps: float, frames_T: int, b_min: int = 1, b_max: int = 8,
+                 forget: float = 1.0, knee_gain: float = 0.05):
+        cfg = sds_slo_config(target_fps, forget, knee_gain, frames_T, b_min, b_max)
+        h = _P()
+        check(lib().sds_slo_create(C.byref(cfg), C.byref(h)))
+        self.h = h.value
+
+    def observe(self, batch: int, latency_s: float) -> None:
+        check(lib().sds_slo_observe(self.h, int(batch), float(latency_s)))
+
+    def choose(self) -> dict:
+        r = sds_slo_choice()
+        check(lib().sds_slo_choose(self.h, C.byref(r)))
+        return {n: getattr(r, n) for n, _ in r._fields_}
+
+    def close(self) -> None:
+        if self.h:
+            lib().sds_slo_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
