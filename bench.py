@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--streams", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cfg-type", type=int, default=None,
+                    help="guidance: 0 none, 1 self-negative R-CFG, 2 supplied negative prediction")
+    ap.add_argument("--update-kind", type=int, default=None,
+                    help="0 predict x0 and re-noise, 1 strided DDPM posterior")
     ap.add_argument("--sweep-streams", type=int, default=0,
                     help="print one line per stream count B = 1..N (same workload, one GPU)")
     return ap.parse_args()
@@ -59,8 +63,12 @@ def workload(args, rank: int = 0) -> dict:
     """The workload one rank serves.  Ranks are independent replicas serving
     their own streams, so each rank draws its inputs from its own seed."""
     over = {}
-    if args.streams:
+    if getattr(args, "streams", None):
         over["streams"] = args.streams
+    if getattr(args, "cfg_type", None) is not None:
+        over["cfg_type"] = args.cfg_type
+    if getattr(args, "update_kind", None) is not None:
+        over["update_kind"] = args.update_kind
     w = W.get_config(args.workload, **over)
     w["seed"] = w["seed"] + 1000 * rank
     return w
@@ -78,7 +86,10 @@ def attn_flops(w: dict) -> float:
 def step_bytes(w: dict, with_ssf: bool, with_motion: bool) -> float:
     """Algorithmic bytes of one K4 launch: every operand read once, every result written once."""
     n, S = w["n"], w["streams"]
-    b = 4.0 * S * w["N_s"] * (5 * n + 2)  # x, x0, eps_c (n), z (n-1), x0_new, eps_new | x_next (n), out
+    # x, eps_c, x0 or eps_neg (n each; no third without guidance), z (n-1),
+    # x0_new, eps_new read | x_next (n), out written
+    per_slot = 5 if w.get("cfg_type", 1) != 0 else 4
+    b = 4.0 * S * w["N_s"] * (per_slot * n + 2)
     if with_ssf:
         b += 4.0 * S * w["ssf_E"] * 3     # frame, reference | reference copy
     if with_motion:
@@ -211,7 +222,7 @@ class Runner:
     def set_bytes(self) -> float:
         w = self.w
         b = 2.0 * w["streams"] * w["q_rows"] * w["HD"] + 2 * 2.0 * w["streams"] * w["kv_rows"] * w["HD"]
-        b += 4.0 * w["streams"] * w["N_s"] * (4 * w["n"] + 1)
+        b += 4.0 * w["streams"] * w["N_s"] * ((5 if w.get("cfg_type", 1) == 2 else 4) * w["n"] + 1)
         if w["ssf"]:
             b += 4.0 * w["streams"] * w["ssf_E"]
         if w["motion"]:
@@ -248,11 +259,12 @@ class Runner:
 
     def io(self, s: dict):
         n = self.w["n"]
+        en = [s["eps_neg"][i] for i in range(n)] if "eps_neg" in s else None
         return self.B.make_step_io([s["x"][i] for i in range(n)], [s["x0"][i] for i in range(n)],
                                    [s["eps_c"][i] for i in range(n)],
                                    [s["z"][i] for i in range(n - 1)], self.x_next, self.out,
                                    s["x0_new"], s["eps_new"], s.get("frame"), s.get("u"),
-                                   s.get("chunk"))
+                                   s.get("chunk"), en)
 
     def step(self, s: dict, ev=None):
         """One pass of the hot path.  ev: optional dict of (start, end) events per kernel."""

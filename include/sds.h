@@ -61,7 +61,7 @@ extern "C" {
 #define SDS_API
 #endif
 
-#define SDS_ABI_VERSION 2
+#define SDS_ABI_VERSION 3
 #define SDS_MAX_SLOTS 8
 #define SDS_MAX_CHUNK_FRAMES 8
 
@@ -102,7 +102,14 @@ typedef enum {
  * beta_start to beta_end; slot i runs at timestep
  * (num_train_steps-1) - t_index[i]*(num_train_steps/num_inference_steps).
  * cfg_type: 0 = no guidance (eps_cfg = eps_c), 1 = self-negative R-CFG with
- * gamma, delta ([SDO] cfg_type="self").
+ * gamma, delta ([SDO] cfg_type="self"), 2 = R-CFG with a supplied negative
+ * prediction per slot (sds_step_io.eps_neg): the onetime-negative variant
+ * ([SD] R-CFG, one negative evaluation; [SDO] cfg_type="initialize"), and,
+ * with delta = 1 and unconditional predictions, standard CFG.
+ * update_kind: 0 = predict x0 and re-noise it to the next slot's level;
+ * 1 = the DDPM ancestral step ([BLOG] section 7) taken between the slot's
+ * timestep t and the next slot's t', with alpha = abar_t / abar_t' and
+ * sigma^2 = (1 - abar_t') / (1 - abar_t) * (1 - alpha) (posterior variance).
  *
  * slot_elems: fp32 elements of one slot latent (T * frame_elems in video).
  * SSF ([SD] SSF, [SDO]): ssf_elems per frame, ssf_eta, max_skip_frame.
@@ -130,6 +137,7 @@ typedef struct {
   int64_t motion_on, frame_elems, mot_k;
   int64_t mem_cap_bytes;
   int64_t attn_ctas;
+  int64_t update_kind;
   double rope_base, s_th, beta_start, beta_end, gamma, delta, ssf_eta;
   double mot_sigma, mot_lambda, s_min, s_max;
 } sds_config;
@@ -151,6 +159,8 @@ typedef struct {
  *             frame in the same pass; ssf_u [S] uniform draws in [0,1)
  *   motion_chunk [S][frames_T][frame_elems] or NULL: update the motion
  *             estimate and noise rate from these latent frames
+ *   eps_neg[i] cfg_type 2 only: slot i's negative (or unconditional)
+ *             noise prediction; slots may share one buffer
  * x0 shifting between steps (slot i+1's x0 is this step's x0[i]) is left to
  * the caller, which can rotate the pointers at no cost.
  */
@@ -166,6 +176,7 @@ typedef struct {
   const float* ssf_frame;
   const float* ssf_u;
   const float* motion_chunk;
+  const float* eps_neg[SDS_MAX_SLOTS];
 } sds_step_io;
 
 /* Per-stream decisions, as of the last completed call that made them. */
@@ -285,11 +296,14 @@ SDS_API sds_status sds_attention(const void* q, const void* k, const void* v, vo
  * K4 -- one fused pass ([SD] "Residual CFG", [BLOG] update, [SD] "SSF",
  * [V2] "Motion-aware noise scheduler").  Per slot i, with a = alphabar of
  * slot i's timestep, in fp32 with host-double coefficients:
- *   eps_neg = (x_i - sqrt(a) x0_i) / sqrt(1 - a)
+ *   eps_neg = (x_i - sqrt(a) x0_i) / sqrt(1 - a)   (cfg_type 1; cfg_type 2:
+ *             the supplied io->eps_neg[i])
  *   eps_cfg = gamma eps_c + delta (1 - gamma) eps_neg   (= the printed
  *             delta eps_neg + gamma (eps_c - delta eps_neg))
  *   x0hat   = (x_i - sqrt(1 - a) eps_cfg) / sqrt(a)
- *   x_next[i+1] = sqrt(a_{i+1}) x0hat + sqrt(1 - a_{i+1}) z_i  (i < n-1)
+ *   x_next[i+1] = sqrt(a_{i+1}) x0hat + sqrt(1 - a_{i+1}) z_i  (i < n-1;
+ *             update_kind 1: (x_i - (1 - al) / sqrt(1 - a) eps_cfg) / sqrt(al)
+ *             + sigma z_i with al = a / a_{i+1})
  *   out = x0hat of slot n-1;  x_next[0] = sqrt(a_0) x0_new + sqrt(1-a_0) eps_new.
  * With io->ssf_frame: the similarity filter of sds_ssf on that frame.
  * With io->motion_chunk: per frame pair the RMS difference d (the previous

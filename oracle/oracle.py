@@ -20,7 +20,7 @@ class OrcCfg(C.Structure):
     _fields_ = [(n, _i64) for n in (
         "n", "T", "L", "H", "d", "M", "R", "image_mode", "rope_on", "grid_h", "grid_w",
         "rope_tau", "D", "n_inf", "n_train", "cfg_type", "N_s", "ssf_E", "max_skip",
-        "N_f", "mot_k")] + [("t_index", _i64 * 8)] + [(n, _f64) for n in (
+        "N_f", "mot_k", "update_kind")] + [("t_index", _i64 * 8)] + [(n, _f64) for n in (
         "rope_base", "s_th", "beta_start", "beta_end", "gamma", "delta", "eta",
         "sigma", "lam", "s_min", "s_max")]
 
@@ -62,6 +62,7 @@ def lib():
         L.orc_rotate_queries.argtypes = [P, P, P]
         L.orc_attend.argtypes = [P, P, P, _i64, P]
         L.orc_step_update.argtypes = [P] * 9
+        L.orc_step_update2.argtypes = [P] * 10
         L.orc_ssf.argtypes = [P, P, C.c_float, P, P]
         L.orc_motion.argtypes = [P, P, P]
         L.orc_set_lazy.argtypes = [P, C.c_int]
@@ -91,6 +92,7 @@ def make_cfg(w: dict) -> OrcCfg:
     c.D, c.n_inf, c.n_train, c.cfg_type = w["D"], w["n_inf"], w["n_train"], w["cfg_type"]
     c.N_s, c.ssf_E, c.max_skip = w["N_s"], w["ssf_E"], w["max_skip"]
     c.N_f, c.mot_k = w["N_f"], w["mot_k"]
+    c.update_kind = w.get("update_kind", 0)
     for i, t in enumerate(w["t_index"]):
         c.t_index[i] = t
     c.rope_base, c.s_th = w["rope_base"], w["s_th"]
@@ -233,17 +235,19 @@ class Stream:
         lib().orc_attend(self.h, _p(q), _p(rows), len(rows), _p(out))
         return out
 
-    def step_update(self, x, x0, eps_c, z, x0_new, eps_new):
-        """Slot arrays [n][N_s] (z: [n-1][N_s]) for this stream; returns (x_next, out)."""
+    def step_update(self, x, x0, eps_c, z, x0_new, eps_new, eps_neg=None):
+        """Slot arrays [n][N_s] (z: [n-1][N_s]) for this stream; eps_neg [n][N_s]
+        for cfg_type 2; returns (x_next, out)."""
         w = self.w
         n, N = w["n"], w["N_s"]
         f = lambda a: np.ascontiguousarray(a, dtype=np.float32)
         x, x0, eps_c, x0_new, eps_new = map(f, (x, x0, eps_c, x0_new, eps_new))
         z = f(z) if n > 1 else np.zeros((1, N), dtype=np.float32)
+        en = f(eps_neg) if eps_neg is not None else np.zeros((n, N), dtype=np.float32)
         xn = np.zeros((n, N), dtype=np.float64)
         out = np.zeros(N, dtype=np.float64)
-        lib().orc_step_update(self.h, _p(x), _p(x0), _p(eps_c), _p(z), _p(x0_new), _p(eps_new),
-                              _p(xn), _p(out))
+        lib().orc_step_update2(self.h, _p(x), _p(x0), _p(eps_c), _p(z), _p(en), _p(x0_new),
+                               _p(eps_new), _p(xn), _p(out))
         return xn, out
 
     def ssf(self, frame: np.ndarray, u: float) -> dict:

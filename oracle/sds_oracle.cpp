@@ -58,6 +58,7 @@ struct orc_cfg {
   long long N_s;                          // elements of one slot latent
   long long ssf_E, max_skip;
   long long N_f, mot_k;
+  long long update_kind;                  // 0: predict x0 then re-noise, 1: strided DDPM posterior
   long long t_index[8];
   double rope_base, s_th, beta_start, beta_end, gamma, delta, eta;
   double sigma, lam, s_min, s_max;
@@ -546,8 +547,26 @@ void orc_attend(void* p, const uint16_t* q, const long long* rows, long long nse
 // 1 - alphabar_t of the slot's own timestep; x0 is the slot's own input
 // latent.  reading: the strided update predicts x0hat, then re-noises it to
 // the next slot's level with the supplied ancestral noise z.
-void orc_step_update(void* p, const float* x, const float* x0, const float* eps_c, const float* z,
-                     const float* x0_new, const float* eps_new, double* x_next, double* out) {
+// a5: R-CFG combine and the stream-batch update of every slot.
+// x, x0, eps_c: float [n][N_s]; z: float [n-1][N_s]; eps_neg: float [n][N_s]
+// (cfg_type 2 only, else may be NULL); x0_new, eps_new: float [N_s];
+// outputs x_next [n][N_s], out [N_s] in double.
+// cfg_type 0: eps_cfg = eps_c.  1 (self-negative R-CFG): eps_neg is the
+// virtual residual (x - sqrt(abar) x0) / sqrt(1 - abar).  2 (onetime-negative
+// R-CFG, or standard CFG with delta = 1): eps_neg is a supplied negative /
+// unconditional prediction.  Both combine as delta*eps_neg +
+// gamma*(eps_c - delta*eps_neg).
+// update_kind 0 (reading: predict x0, re-noise to the next slot's level):
+//   x_next[i+1] = sqrt(abar') x0hat + sqrt(1 - abar') z_i.
+// update_kind 1 (the blog's DDPM ancestral step taken between the slot's
+// timestep t and the next slot's t', reading: alpha = abar_t / abar_t' and
+// sigma^2 the posterior variance (1 - abar_t') / (1 - abar_t) (1 - alpha)):
+//   x_next[i+1] = (x - (1 - alpha) / sqrt(1 - abar_t) eps_cfg) / sqrt(alpha) + sigma z_i.
+// The last slot's x0hat is the completed frame; the incoming frame enters
+// slot 0 as sqrt(abar_0) x0_new + sqrt(1 - abar_0) eps_new.
+void orc_step_update2(void* p, const float* x, const float* x0, const float* eps_c, const float* z,
+                      const float* eps_neg, const float* x0_new, const float* eps_new,
+                      double* x_next, double* out) {
   Stream* s = (Stream*)p;
   const orc_cfg& c = s->c;
   long long N = c.N_s;
@@ -556,19 +575,28 @@ void orc_step_update(void* p, const float* x, const float* x0, const float* eps_
     double ab_next = (i + 1 < c.n) ? s->abar[(size_t)slot_timestep(c, i + 1)] : 0.0;
     for (long long e = 0; e < N; ++e) {
       size_t k = (size_t)(i * N + e);
-      double xv = x[k], x0v = x0[k], ec = eps_c[k];
+      double xv = x[k], ec = eps_c[k];
       double eps_cfg = ec;
-      if (c.cfg_type == 1) {
-        double eps_neg = (xv - std::sqrt(ab) * x0v) / std::sqrt(1.0 - ab);
+      if (c.cfg_type == 1 || c.cfg_type == 2) {
+        double en = (c.cfg_type == 1) ? (xv - std::sqrt(ab) * (double)x0[k]) / std::sqrt(1.0 - ab)
+                                       : (double)eps_neg[k];
         // The printed combine delta*eps_neg + gamma*(eps_c - delta*eps_neg),
         // regrouped as gamma*eps_c + delta*(1-gamma)*eps_neg (equal in real
         // arithmetic) so that gamma = 1 returns eps_c exactly.
-        eps_cfg = c.gamma * ec + c.delta * (1.0 - c.gamma) * eps_neg;
+        eps_cfg = c.gamma * ec + c.delta * (1.0 - c.gamma) * en;
       }
       double x0hat = (xv - std::sqrt(1.0 - ab) * eps_cfg) / std::sqrt(ab);
       if (i + 1 < c.n) {
-        x_next[(size_t)((i + 1) * N + e)] =
-            std::sqrt(ab_next) * x0hat + std::sqrt(1.0 - ab_next) * (double)z[k];
+        double nx;
+        if (c.update_kind == 1) {
+          double alpha = ab / ab_next;
+          double sigma = std::sqrt((1.0 - ab_next) / (1.0 - ab) * (1.0 - alpha));
+          nx = (xv - (1.0 - alpha) / std::sqrt(1.0 - ab) * eps_cfg) / std::sqrt(alpha) +
+               sigma * (double)z[k];
+        } else {
+          nx = std::sqrt(ab_next) * x0hat + std::sqrt(1.0 - ab_next) * (double)z[k];
+        }
+        x_next[(size_t)((i + 1) * N + e)] = nx;
       } else {
         out[e] = x0hat;
       }
@@ -577,6 +605,11 @@ void orc_step_update(void* p, const float* x, const float* x0, const float* eps_
   double ab0 = s->abar[(size_t)slot_timestep(c, 0)];
   for (long long e = 0; e < N; ++e)
     x_next[e] = std::sqrt(ab0) * (double)x0_new[e] + std::sqrt(1.0 - ab0) * (double)eps_new[e];
+}
+
+void orc_step_update(void* p, const float* x, const float* x0, const float* eps_c, const float* z,
+                     const float* x0_new, const float* eps_new, double* x_next, double* out) {
+  orc_step_update2(p, x, x0, eps_c, z, nullptr, x0_new, eps_new, x_next, out);
 }
 
 // a6: stochastic similarity filter on one incoming frame.

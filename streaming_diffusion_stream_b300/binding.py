@@ -13,7 +13,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsds.so")
 
-SDS_ABI_VERSION = 2
+SDS_ABI_VERSION = 3
 SDS_MAX_SLOTS = 8
 SDS_MAX_CHUNK_FRAMES = 8
 SDS_STATE_MAGIC = b"SDSSTAT1"
@@ -35,7 +35,7 @@ class sds_config(C.Structure):
         ("t_index", _i64 * SDS_MAX_SLOTS)] + [(n, _i64) for n in (
             "num_inference_steps", "num_train_steps", "cfg_type", "slot_elems", "ssf_on",
             "ssf_elems", "max_skip_frame", "motion_on", "frame_elems", "mot_k",
-            "mem_cap_bytes", "attn_ctas")] + [(n, _f64) for n in (
+            "mem_cap_bytes", "attn_ctas", "update_kind")] + [(n, _f64) for n in (
                 "rope_base", "s_th", "beta_start", "beta_end", "gamma", "delta", "ssf_eta",
                 "mot_sigma", "mot_lambda", "s_min", "s_max")]
 
@@ -44,7 +44,8 @@ class sds_step_io(C.Structure):
     _fields_ = [("x", _P * SDS_MAX_SLOTS), ("x0", _P * SDS_MAX_SLOTS),
                 ("eps_c", _P * SDS_MAX_SLOTS), ("z", _P * SDS_MAX_SLOTS),
                 ("x_next", _P * SDS_MAX_SLOTS), ("out", _P), ("x0_new", _P), ("eps_new", _P),
-                ("ssf_frame", _P), ("ssf_u", _P), ("motion_chunk", _P)]
+                ("ssf_frame", _P), ("ssf_u", _P), ("motion_chunk", _P),
+                ("eps_neg", _P * SDS_MAX_SLOTS)]
 
 
 class sds_stream_state(C.Structure):
@@ -180,6 +181,7 @@ def config_from_workload(w: dict, mem_cap_bytes: int = 0) -> sds_config:
     c.motion_on, c.frame_elems, c.mot_k = int(w["motion"]), w["N_f"], w["mot_k"]
     c.mem_cap_bytes = mem_cap_bytes
     c.attn_ctas = w.get("attn_ctas", 0)
+    c.update_kind = w.get("update_kind", 0)
     c.rope_base, c.s_th = w["rope_base"], w["s_th"]
     c.beta_start, c.beta_end = w["beta_start"], w["beta_end"]
     c.gamma, c.delta, c.ssf_eta = w["gamma"], w["delta"], w["eta"]
@@ -224,8 +226,9 @@ def sds_attention(q, k, v, o, S, Lq, Lk, H, head_dim, stream=None):
 
 
 def make_step_io(x, x0, eps_c, z, x_next, out, x0_new, eps_new, ssf_frame=None, ssf_u=None,
-                 motion_chunk=None) -> sds_step_io:
-    """x, x0, eps_c, x_next: sequences of n per-slot tensors; z: n-1 tensors."""
+                 motion_chunk=None, eps_neg=None) -> sds_step_io:
+    """x, x0, eps_c, x_next: sequences of n per-slot tensors; z: n-1 tensors;
+    eps_neg: n tensors (cfg_type 2) or None."""
     io = sds_step_io()
     for i, t in enumerate(x):
         io.x[i] = _ptr(t)
@@ -239,6 +242,8 @@ def make_step_io(x, x0, eps_c, z, x_next, out, x0_new, eps_new, ssf_frame=None, 
         io.x_next[i] = _ptr(t)
     io.out, io.x0_new, io.eps_new = _ptr(out), _ptr(x0_new), _ptr(eps_new)
     io.ssf_frame, io.ssf_u, io.motion_chunk = _ptr(ssf_frame), _ptr(ssf_u), _ptr(motion_chunk)
+    for i, t in enumerate(eps_neg or []):
+        io.eps_neg[i] = _ptr(t)
     return io
 
 

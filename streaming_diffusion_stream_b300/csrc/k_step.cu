@@ -69,20 +69,40 @@ __device__ __forceinline__ void block_sum3(dfloat& a, dfloat& b, dfloat& c, dflo
 __device__ __forceinline__ float4 ld4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
-__device__ __forceinline__ float x0hat1(float x, float x0, float ec, float sa, float inv_s1a,
-                                        float s1a, float inv_sa, float g, float dg) {
-  const float en = __fmaf_rn(-sa, x0, x) * inv_s1a;
-  const float ecfg = __fmaf_rn(g, ec, dg * en);
-  return __fmaf_rn(-s1a, ecfg, x) * inv_sa;
+// eps_cfg = gamma eps_c + delta (1 - gamma) eps_neg with eps_neg the virtual
+// residual (x - sqrt(abar) x0) / sqrt(1 - abar) (cfg_kind 1) or the supplied
+// prediction (cfg_kind 2); eps_c alone without guidance.
+__device__ __forceinline__ float eps_cfg1(float x, float neg, float ec, float sa, float inv_s1a,
+                                          float g, float dg, int kind) {
+  const float en = kind == 1 ? __fmaf_rn(-sa, neg, x) * inv_s1a : neg;
+  return __fmaf_rn(g, ec, dg * en);
 }
 
-__device__ __forceinline__ float4 x0hat4(float4 x, float4 x0, float4 ec, const StepParams& p,
-                                         int i) {
-  const float sa = p.c_sa[i], a = p.c_inv_s1a[i], b = p.c_s1a[i], c = p.c_inv_sa[i];
-  return make_float4(x0hat1(x.x, x0.x, ec.x, sa, a, b, c, p.c_gamma, p.c_dg),
-                     x0hat1(x.y, x0.y, ec.y, sa, a, b, c, p.c_gamma, p.c_dg),
-                     x0hat1(x.z, x0.z, ec.z, sa, a, b, c, p.c_gamma, p.c_dg),
-                     x0hat1(x.w, x0.w, ec.w, sa, a, b, c, p.c_gamma, p.c_dg));
+__device__ __forceinline__ float4 eps_cfg4(float4 x, float4 neg, float4 ec, const StepParams& p,
+                                           int i) {
+  if (p.cfg_kind == 0) return ec;
+  const float sa = p.c_sa[i], a = p.c_inv_s1a[i];
+  return make_float4(eps_cfg1(x.x, neg.x, ec.x, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.y, neg.y, ec.y, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.z, neg.z, ec.z, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.w, neg.w, ec.w, sa, a, p.c_gamma, p.c_dg, p.cfg_kind));
+}
+
+// x0hat = (x - sqrt(1 - abar) eps_cfg) / sqrt(abar)
+__device__ __forceinline__ float4 x0hat4(float4 x, float4 ecfg, const StepParams& p, int i) {
+  const float b = p.c_s1a[i], c = p.c_inv_sa[i];
+  return make_float4(__fmaf_rn(-b, ecfg.x, x.x) * c, __fmaf_rn(-b, ecfg.y, x.y) * c,
+                     __fmaf_rn(-b, ecfg.z, x.z) * c, __fmaf_rn(-b, ecfg.w, x.w) * c);
+}
+
+// the strided DDPM step: x / sqrt(alpha) - c_pe eps_cfg + sigma z
+__device__ __forceinline__ float4 ddpm4(float4 x, float4 ecfg, float4 z, const StepParams& p,
+                                        int i) {
+  const float cx = p.c_px[i], ce = p.c_pe[i], sg = p.c_sig[i];
+  return make_float4(__fmaf_rn(sg, z.x, __fmaf_rn(-ce, ecfg.x, cx * x.x)),
+                     __fmaf_rn(sg, z.y, __fmaf_rn(-ce, ecfg.y, cx * x.y)),
+                     __fmaf_rn(sg, z.z, __fmaf_rn(-ce, ecfg.z, cx * x.z)),
+                     __fmaf_rn(sg, z.w, __fmaf_rn(-ce, ecfg.w, cx * x.w)));
 }
 
 __device__ __forceinline__ float4 noise4(float4 a, float4 b, float ca, float cb) {
@@ -99,20 +119,26 @@ __device__ void update_block(const StepParams& p, int64_t w) {
   const int64_t el = b * kUpdBlockElems + threadIdx.x * 4;
   if (el >= p.N_s) return;
   const int64_t e = s * p.N_s + el;
-  float4 x[N], x0[N], ec[N], z[N > 1 ? N - 1 : 1];
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  // second operand of the negative branch: x0 (self-negative) or the
+  // supplied negative prediction; not read without guidance
+  float4 x[N], neg[N], ec[N], z[N > 1 ? N - 1 : 1];
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     x[i] = ld4(p.x[i] + e);
-    x0[i] = ld4(p.x0[i] + e);
+    neg[i] = p.cfg_kind == 0 ? zero4 : ld4((p.cfg_kind == 2 ? p.eps_neg[i] : p.x0[i]) + e);
     ec[i] = ld4(p.eps_c[i] + e);
     if (i < N - 1) z[i] = ld4(p.z[i] + e);
   }
   const float4 xn = ld4(p.x0_new + e), en = ld4(p.eps_new + e);
 #pragma unroll
   for (int i = N - 1; i >= 0; --i) {
-    const float4 xh = x0hat4(x[i], x0[i], ec[i], p, i);
+    const float4 ecfg = eps_cfg4(x[i], neg[i], ec[i], p, i);
+    const float4 xh = x0hat4(x[i], ecfg, p, i);
     if (i == N - 1) {
       st4(p.out + e, xh);
+    } else if (p.upd_kind == 1) {
+      st4(p.x_next[i + 1] + e, ddpm4(x[i], ecfg, z[i], p, i));
     } else {
       st4(p.x_next[i + 1] + e, noise4(xh, z[i], p.c_sa[i + 1], p.c_s1a[i + 1]));
     }

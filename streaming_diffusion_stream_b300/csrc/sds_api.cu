@@ -119,7 +119,10 @@ sds_status validate(const sds_config* c, std::string& why) {
     if (c->t_index[i] < 0 || t < 0 || t >= c->num_train_steps)
       return bad("t_index entry maps outside the training schedule");
   }
-  if (c->cfg_type != 0 && c->cfg_type != 1) return bad("cfg_type must be 0 (none) or 1 (self)");
+  if (c->cfg_type < 0 || c->cfg_type > 2)
+    return bad("cfg_type must be 0 (none), 1 (self-negative) or 2 (supplied negative)");
+  if (c->update_kind != 0 && c->update_kind != 1)
+    return bad("update_kind must be 0 (re-noise x0hat) or 1 (strided DDPM posterior)");
   if (c->attn_ctas < 0 || c->attn_ctas > kAttnMaxCtas) return bad("attn_ctas must be in [0, 160]");
   if (c->slot_elems < 4 || c->slot_elems % 4 != 0) return bad("slot_elems must be a positive multiple of 4");
   if (c->ssf_on) {
@@ -647,8 +650,11 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
   const int n = (int)c.slots_n;
   auto okp = [](const void* p) { return p && aligned16(p); };
   for (int i = 0; i < n; ++i) {
-    if (!okp(io->x[i]) || !okp(io->x0[i]) || !okp(io->eps_c[i]) || !okp(io->x_next[i]))
-      return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: slot %d arrays must be non-NULL and 16-byte aligned", i);
+    if (!okp(io->x[i]) || !okp(io->eps_c[i]) || !okp(io->x_next[i]) ||
+        (c.cfg_type == 1 && !okp(io->x0[i])) || (c.cfg_type == 2 && !okp(io->eps_neg[i])))
+      return fail(ctx, SDS_ERR_INVALID_ARG,
+                  "step_update: slot %d arrays (x, eps_c, x_next, and x0 for cfg_type 1 or eps_neg "
+                  "for cfg_type 2) must be non-NULL and 16-byte aligned", i);
     if (i < n - 1 && !okp(io->z[i]))
       return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: z[%d] must be non-NULL and 16-byte aligned", i);
   }
@@ -677,8 +683,19 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
     p.c_inv_s1a[i] = (float)(1.0 / std::sqrt(1.0 - a));
     p.c_s1a[i] = (float)std::sqrt(1.0 - a);
     p.c_inv_sa[i] = (float)(1.0 / std::sqrt(a));
+    p.eps_neg[i] = c.cfg_type == 2 ? io->eps_neg[i] : nullptr;
+    if (i + 1 < n) {
+      // strided DDPM step from this slot's timestep to the next slot's
+      const double an = ctx->abar_slot[i + 1];
+      const double al = a / an;
+      p.c_px[i] = (float)(1.0 / std::sqrt(al));
+      p.c_pe[i] = (float)((1.0 - al) / (std::sqrt(al) * std::sqrt(1.0 - a)));
+      p.c_sig[i] = (float)std::sqrt((1.0 - an) / (1.0 - a) * (1.0 - al));
+    }
   }
-  if (c.cfg_type == 1) {
+  p.cfg_kind = (int32_t)c.cfg_type;
+  p.upd_kind = (int32_t)c.update_kind;
+  if (c.cfg_type != 0) {
     p.c_gamma = (float)c.gamma;
     p.c_dg = (float)(c.delta * (1.0 - c.gamma));
   } else {

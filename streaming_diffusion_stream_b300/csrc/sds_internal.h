@@ -121,6 +121,12 @@ struct StepParams {
   float c_s1a[SDS_MAX_SLOTS];      // sqrt(1 - abar_i)
   float c_inv_sa[SDS_MAX_SLOTS];   // 1 / sqrt(abar_i)
   float c_gamma, c_dg;             // gamma, delta * (1 - gamma)
+  const float* eps_neg[SDS_MAX_SLOTS];  // supplied negative predictions (cfg_kind 2)
+  int32_t cfg_kind;                // 0 none, 1 self-negative (from x0), 2 supplied eps_neg
+  int32_t upd_kind;                // 0 x0hat re-noised, 1 strided DDPM posterior
+  float c_px[SDS_MAX_SLOTS];       // DDPM: 1 / sqrt(alpha_i)
+  float c_pe[SDS_MAX_SLOTS];       // DDPM: (1 - alpha_i) / (sqrt(alpha_i) sqrt(1 - abar_i))
+  float c_sig[SDS_MAX_SLOTS];      // DDPM: sigma_i
   int32_t n;                       // slots (0: no update segment)
   int64_t N_s;
   // SSF segment

@@ -23,6 +23,7 @@ import numpy as np
 # purpose ids for the counter-based streams
 _P_Q, _P_K, _P_V, _P_X, _P_X0, _P_EPSC, _P_Z, _P_X0NEW, _P_EPSNEW = range(9)
 _P_U, _P_SSF, _P_EMB, _P_LAT, _P_JUMP, _P_BURST, _P_MISC = range(9, 16)
+_P_EPSNEG = 16
 
 _BASE = dict(
     streams=1,
@@ -32,7 +33,8 @@ _BASE = dict(
     n_train=1000,
     beta_start=0.00085,
     beta_end=0.012,
-    cfg_type=1,          # 1 = self-negative R-CFG
+    cfg_type=1,          # 1 = self-negative R-CFG, 2 = supplied negative prediction
+    update_kind=0,       # 0 = predict x0 then re-noise, 1 = strided DDPM posterior
     gamma=1.4,
     delta=1.0,
     s_th=0.9,
@@ -189,6 +191,8 @@ def gen_latents(cfg: dict, step: int) -> dict:
         x0_new=normal_f32(sd, _P_X0NEW, (S, N), step),
         eps_new=normal_f32(sd, _P_EPSNEW, (S, N), step),
     )
+    if cfg.get("cfg_type", 1) == 2:  # a supplied negative / unconditional prediction per slot
+        out["eps_neg"] = normal_f32(sd, _P_EPSNEG, (n, S, N), step)
     return out
 
 

@@ -84,7 +84,8 @@ def _create_status(cfg):
     ("grid_w", 7, "grid_h * grid_w"),
     ("slot_elems", 1022, "slot_elems"),
     ("mot_k", 65, "mot_k"),
-    ("cfg_type", 2, "cfg_type"),
+    ("cfg_type", 3, "cfg_type"),
+    ("update_kind", 2, "update_kind"),
     ("streams", 0, "streams"),
 ])
 def test_invalid_configs_are_rejected_on_the_host(field, value, msg):

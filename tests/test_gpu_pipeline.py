@@ -147,6 +147,21 @@ def test_c1_split_key_schedule_with_sink_fill():
     run_sequence(w, 6)
 
 
+@pytest.mark.parametrize("cfg_type,update_kind,n", [(2, 0, 2), (2, 1, 4), (1, 1, 3), (0, 1, 2)])
+def test_guidance_and_update_variants(cfg_type, update_kind, n):
+    """Onetime-negative R-CFG (supplied negative prediction), the strided DDPM
+    posterior update and their combinations against the oracle."""
+    t_index = [0, 16, 32, 45][:n] if n > 2 else [32, 45]
+    w = W.get_config("c1_tiny", cfg_type=cfg_type, update_kind=update_kind, n=n,
+                     t_index=t_index, steps=4)
+    run_sequence(w, 4)
+
+
+def test_c4_full_size_ddpm_update_with_supplied_negative():
+    w = W.get_config("c4_dit14b_video", cfg_type=2, update_kind=1)
+    run_sequence(w, 2, rows_per_step=8, attend_every=2, check_kv_every=2)
+
+
 def test_rope_reset_fires_with_small_tau():
     w = W.get_config("c1_tiny", rope_tau=3, steps=11)
     stats = run_sequence(w, 11)

@@ -534,3 +534,90 @@ def test_lazy_provenance_then_materialize_equals_eager_push():
     kl, vl = lazy.kv()
     assert np.array_equal(ke, kl) and np.array_equal(ve, vl)
     assert np.array_equal(eager.emb(), lazy.emb())
+
+
+# --------------------------------------------------------------- guidance / update variants
+
+def _slot_inputs(w, rng):
+    n, N = w["n"], w["N_s"]
+    return dict(x=rng.standard_normal((n, N)).astype(np.float32),
+                x0=rng.standard_normal((n, N)).astype(np.float32),
+                eps_c=rng.standard_normal((n, N)).astype(np.float32),
+                z=rng.standard_normal((max(n - 1, 1), N)).astype(np.float32)[: max(n - 1, 0)],
+                x0_new=rng.standard_normal(N).astype(np.float32),
+                eps_new=rng.standard_normal(N).astype(np.float32),
+                eps_neg=rng.standard_normal((n, N)).astype(np.float32))
+
+
+def test_supplied_negative_with_delta_one_is_standard_cfg():
+    """cfg_type 2, delta = 1, eps_neg = the unconditional prediction eps_u:
+    eps_cfg must be eps_u + gamma (eps_c - eps_u), seen through x0hat of the
+    completed slot."""
+    w = tiny(cfg_type=2, delta=1.0, gamma=1.7, n=2)
+    st = O.Stream(w)
+    d = _slot_inputs(w, np.random.default_rng(3))
+    xn, out = st.step_update(d["x"], d["x0"], d["eps_c"], d["z"], d["x0_new"], d["eps_new"],
+                             eps_neg=d["eps_neg"])
+    ab = O.alpha_bar(w)[O.slot_timestep(w, 1)]
+    eu, ec, x = (d[k][1].astype(np.float64) for k in ("eps_neg", "eps_c", "x"))
+    cfg = eu + 1.7 * (ec - eu)
+    assert np.allclose(out, (x - math.sqrt(1 - ab) * cfg) / math.sqrt(ab), rtol=1e-12, atol=1e-12)
+
+
+def test_supplied_virtual_residual_reproduces_self_negative():
+    """Feeding the virtual residual as the supplied negative gives the
+    self-negative result: the two guidance paths use eps_neg in one role."""
+    d = _slot_inputs(tiny(n=2), np.random.default_rng(4))
+    w_self, w_sup = tiny(n=2, cfg_type=1), tiny(n=2, cfg_type=2)
+    ab = O.alpha_bar(w_self)
+    res = np.stack([(d["x"][i].astype(np.float64) - math.sqrt(ab[O.slot_timestep(w_self, i)]) * d["x0"][i])
+                    / math.sqrt(1 - ab[O.slot_timestep(w_self, i)]) for i in range(2)])
+    a = O.Stream(w_self).step_update(d["x"], d["x0"], d["eps_c"], d["z"], d["x0_new"], d["eps_new"])
+    # the residual rounds to float32 on its way in: compare within that rounding
+    b = O.Stream(w_sup).step_update(d["x"], d["x0"], d["eps_c"], d["z"], d["x0_new"], d["eps_new"],
+                                    eps_neg=res.astype(np.float32))
+    assert np.allclose(a[0], b[0], rtol=1e-6, atol=1e-6) and np.allclose(a[1], b[1], rtol=1e-6, atol=1e-6)
+
+
+def test_ddpm_update_mean_is_the_posterior_mean():
+    """update_kind 1 with the true noise and z = 0 lands on the DDPM posterior
+    mean of q(x_t' | x_t, x0) written in its x0 / x_t form."""
+    w = tiny(n=2, cfg_type=0, update_kind=1)
+    rng = np.random.default_rng(5)
+    N = w["N_s"]
+    ab = O.alpha_bar(w)
+    t0, t1 = O.slot_timestep(w, 0), O.slot_timestep(w, 1)
+    a_t, a_n = ab[t0], ab[t1]
+    x0 = rng.standard_normal((2, N))
+    eps = rng.standard_normal((2, N))
+    xt = np.sqrt(np.array([a_t, ab[t1]]))[:, None] * x0 + np.sqrt(1 - np.array([a_t, ab[t1]]))[:, None] * eps
+    f32 = lambda v: v.astype(np.float32)
+    xt32, eps32, x032 = f32(xt), f32(eps), f32(x0)
+    xn, _ = O.Stream(w).step_update(xt32, x032, eps32, np.zeros((1, N), np.float32),
+                                    f32(x0[0]), f32(eps[0]))
+    al = a_t / a_n
+    mu = (math.sqrt(a_n) * (1 - al) / (1 - a_t)) * x032[0].astype(np.float64) + \
+         (math.sqrt(al) * (1 - a_n) / (1 - a_t)) * xt32[0].astype(np.float64)
+    # the true noise of the rounded x_t differs from eps by the rounding: loose on that
+    assert np.allclose(xn[1], mu, rtol=0, atol=5e-6)
+
+
+def test_ddpm_adjacent_step_noise_scale_is_beta_tilde():
+    """With adjacent timesteps the noise scale of update_kind 1 is the DDPM
+    posterior standard deviation sqrt((1 - abar_{t-1}) / (1 - abar_t) beta_t),
+    beta_t taken straight from the scaled-linear definition."""
+    w = tiny(n=2, cfg_type=0, update_kind=1, n_inf=1000, t_index=[5, 6])
+    t0, t1 = O.slot_timestep(w, 0), O.slot_timestep(w, 1)
+    assert t0 - t1 == 1
+    N = w["N_s"]
+    x = np.ones((2, N), np.float32)
+    e = np.zeros((2, N), np.float32)
+    z1 = np.ones((1, N), np.float32)
+    st = O.Stream(w)
+    a = st.step_update(x, x, e, z1, x[0], e[0])[0][1]
+    b = st.step_update(x, x, e, np.zeros_like(z1), x[0], e[0])[0][1]
+    sb, eb = math.sqrt(w["beta_start"]), math.sqrt(w["beta_end"])
+    beta = (sb + t0 * (eb - sb) / (w["n_train"] - 1)) ** 2
+    ab = O.alpha_bar(w)
+    sigma = math.sqrt((1 - ab[t1]) / (1 - ab[t0]) * beta)
+    assert np.allclose(a - b, sigma, rtol=1e-10)
