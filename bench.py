@@ -54,6 +54,8 @@ def parse():
                     help="guidance: 0 none, 1 self-negative R-CFG, 2 supplied negative prediction")
     ap.add_argument("--update-kind", type=int, default=None,
                     help="0 predict x0 and re-noise, 1 strided DDPM posterior")
+    ap.add_argument("--noise-rate-on", action="store_true",
+                    help="the incoming frame enters slot 0 at the motion noise rate")
     ap.add_argument("--sweep-streams", type=int, default=0,
                     help="print one line per stream count B = 1..N (same workload, one GPU)")
     return ap.parse_args()
@@ -69,6 +71,8 @@ def workload(args, rank: int = 0) -> dict:
         over["cfg_type"] = args.cfg_type
     if getattr(args, "update_kind", None) is not None:
         over["update_kind"] = args.update_kind
+    if getattr(args, "noise_rate_on", False):
+        over["noise_rate_on"] = 1
     w = W.get_config(args.workload, **over)
     w["seed"] = w["seed"] + 1000 * rank
     return w

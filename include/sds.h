@@ -61,7 +61,7 @@ extern "C" {
 #define SDS_API
 #endif
 
-#define SDS_ABI_VERSION 3
+#define SDS_ABI_VERSION 4
 #define SDS_MAX_SLOTS 8
 #define SDS_MAX_CHUNK_FRAMES 8
 
@@ -106,6 +106,14 @@ typedef enum {
  * prediction per slot (sds_step_io.eps_neg): the onetime-negative variant
  * ([SD] R-CFG, one negative evaluation; [SDO] cfg_type="initialize"), and,
  * with delta = 1 and unconditional predictions, standard CFG.
+ * noise_rate_on: 1 applies the motion-aware noise rate s ([V2] "Motion-aware
+ * noise scheduler": the rate adapts the denoising path to the motion) to
+ * the incoming frame: it enters slot 0 at timestep t_s = round(s *
+ * (num_train_steps - 1)) instead of slot 0's fixed timestep, with the rate
+ * decided by the previous step, and the next update treats that frame at
+ * t_s (needs motion_on; sds_stream_state.slot0_timestep reports t_s).
+ * With update_kind 1, round(s_min * (num_train_steps - 1)) must not fall
+ * below slot 1's timestep (else SDS_ERR_INVALID_ARG).
  * update_kind: 0 = predict x0 and re-noise it to the next slot's level;
  * 1 = the DDPM ancestral step ([BLOG] section 7) taken between the slot's
  * timestep t and the next slot's t', with alpha = abar_t / abar_t' and
@@ -138,6 +146,7 @@ typedef struct {
   int64_t mem_cap_bytes;
   int64_t attn_ctas;
   int64_t update_kind;
+  int64_t noise_rate_on;
   double rope_base, s_th, beta_start, beta_end, gamma, delta, ssf_eta;
   double mot_sigma, mot_lambda, s_min, s_max;
 } sds_config;
@@ -196,6 +205,7 @@ typedef struct {
   double noise_rate;      /* EMA noise rate s */
   double motion_d[SDS_MAX_CHUNK_FRAMES]; /* last chunk's pair motions (NaN if absent) */
   int64_t error_word;     /* nonzero: a kernel met an impossible condition */
+  int64_t slot0_timestep; /* timestep of the frame now in slot 0 */
 } sds_stream_state;
 
 /* Host-side ring metadata (identical for all streams of a context). */
@@ -367,9 +377,10 @@ SDS_API sds_status sds_ssf_noalloc(const float* frame, const float* ref, const f
 /*
  * Checkpoints.  A checkpoint is an sds_state_header followed by a payload of
  * 8-byte aligned sections, in this order:
- *   meta      int64[8]: frames pushed F, RoPE offset o, last chunk start p0,
- *             first frame of the last chunk, sinks filled, RoPE resets,
- *             chunks pushed, motion updates done
+ *   meta      int64[16]: frames pushed F, RoPE offset o, last chunk start
+ *             p0, first frame of the last chunk, sinks filled, RoPE resets,
+ *             chunks pushed, motion updates done, update steps done, then
+ *             zeros
  *   records   S per-stream device records (devstate_bytes each; the public
  *             sds_stream_state first, then private SSF / motion fields)
  *   sink_emb  fp32 [S][M][D]
@@ -381,7 +392,7 @@ SDS_API sds_status sds_ssf_noalloc(const float* frame, const float* ref, const f
  * created with a byte-identical sds_config.
  */
 #define SDS_STATE_MAGIC "SDSSTAT1"
-#define SDS_STATE_RECORD_BYTES 720 /* devstate_bytes of this ABI version */
+#define SDS_STATE_RECORD_BYTES 760 /* devstate_bytes of this ABI version */
 typedef struct {
   char magic[8];           /* SDS_STATE_MAGIC without its terminating NUL */
   int64_t abi_version;     /* SDS_ABI_VERSION of the writer */

@@ -20,7 +20,7 @@ class OrcCfg(C.Structure):
     _fields_ = [(n, _i64) for n in (
         "n", "T", "L", "H", "d", "M", "R", "image_mode", "rope_on", "grid_h", "grid_w",
         "rope_tau", "D", "n_inf", "n_train", "cfg_type", "N_s", "ssf_E", "max_skip",
-        "N_f", "mot_k", "update_kind")] + [("t_index", _i64 * 8)] + [(n, _f64) for n in (
+        "N_f", "mot_k", "update_kind", "noise_rate_on")] + [("t_index", _i64 * 8)] + [(n, _f64) for n in (
         "rope_base", "s_th", "beta_start", "beta_end", "gamma", "delta", "eta",
         "sigma", "lam", "s_min", "s_max")]
 
@@ -68,6 +68,8 @@ def lib():
         L.orc_set_lazy.argtypes = [P, C.c_int]
         L.orc_provenance.argtypes = [P, P]
         L.orc_materialize.argtypes = [P, P, P]
+        L.orc_slot0_timestep.restype = _i64
+        L.orc_slot0_timestep.argtypes = [P]
         L.orc_noise_rate.restype = _f64
         L.orc_noise_rate.argtypes = [P]
         L.orc_skip_count.restype = _i64
@@ -93,6 +95,7 @@ def make_cfg(w: dict) -> OrcCfg:
     c.N_s, c.ssf_E, c.max_skip = w["N_s"], w["ssf_E"], w["max_skip"]
     c.N_f, c.mot_k = w["N_f"], w["mot_k"]
     c.update_kind = w.get("update_kind", 0)
+    c.noise_rate_on = w.get("noise_rate_on", 0)
     for i, t in enumerate(w["t_index"]):
         c.t_index[i] = t
     c.rope_base, c.s_th = w["rope_base"], w["s_th"]
@@ -267,6 +270,9 @@ class Stream:
 
     def noise_rate(self) -> float:
         return float(lib().orc_noise_rate(self.h))
+
+    def slot0_timestep(self) -> int:
+        return int(lib().orc_slot0_timestep(self.h))
 
     def set_lazy(self, on: bool = True) -> None:
         """Pushes record provenance only; K/V are built later by materialize()."""

@@ -59,6 +59,7 @@ struct orc_cfg {
   long long ssf_E, max_skip;
   long long N_f, mot_k;
   long long update_kind;                  // 0: predict x0 then re-noise, 1: strided DDPM posterior
+  long long noise_rate_on;                // 1: the incoming frame enters at round(s (N-1))
   long long t_index[8];
   double rope_base, s_th, beta_start, beta_end, gamma, delta, eta;
   double sigma, lam, s_min, s_max;
@@ -201,6 +202,7 @@ struct Stream {
   int has_prev = 0;
   std::vector<double> window;
   double s_rate = 0.0;
+  long long slot0_t = -1;   // timestep of the frame in slot 0 (noise-rate application)
   // lazy mode: pushes record where each key frame came from instead of
   // rotating it; materialize later applies the push arithmetic to the frames
   int lazy = 0;
@@ -287,6 +289,7 @@ void* orc_create(const orc_cfg* c) {
   s->prev.assign((size_t)c->N_f, 0.0f);
   s->s_rate = c->s_min;
   s->prov.assign((size_t)(key_frames(*c) * 3), -1);
+  s->slot0_t = slot_timestep(*c, 0);
   return s;
 }
 
@@ -570,8 +573,18 @@ void orc_step_update2(void* p, const float* x, const float* x0, const float* eps
   Stream* s = (Stream*)p;
   const orc_cfg& c = s->c;
   long long N = c.N_s;
+  // reading of the motion-aware noise scheduler: the noise rate s chooses
+  // the timestep at which the incoming frame enters slot 0,
+  // round(s (N_train - 1)); the frame then in slot 0 sits at the timestep it
+  // entered at.  The rate is the one in force before this step's motion.
+  long long t_new = slot_timestep(c, 0);
+  if (c.noise_rate_on) {
+    t_new = (long long)std::floor(s->s_rate * (double)(c.n_train - 1) + 0.5);
+    t_new = std::min(std::max(t_new, 0LL), c.n_train - 1);
+  }
   for (long long i = 0; i < c.n; ++i) {
-    double ab = s->abar[(size_t)slot_timestep(c, i)];
+    long long ti = (i == 0 && c.noise_rate_on) ? s->slot0_t : slot_timestep(c, i);
+    double ab = s->abar[(size_t)ti];
     double ab_next = (i + 1 < c.n) ? s->abar[(size_t)slot_timestep(c, i + 1)] : 0.0;
     for (long long e = 0; e < N; ++e) {
       size_t k = (size_t)(i * N + e);
@@ -602,10 +615,13 @@ void orc_step_update2(void* p, const float* x, const float* x0, const float* eps
       }
     }
   }
-  double ab0 = s->abar[(size_t)slot_timestep(c, 0)];
+  double ab0 = s->abar[(size_t)t_new];
   for (long long e = 0; e < N; ++e)
     x_next[e] = std::sqrt(ab0) * (double)x0_new[e] + std::sqrt(1.0 - ab0) * (double)eps_new[e];
+  s->slot0_t = t_new;
 }
+
+long long orc_slot0_timestep(void* p) { return ((Stream*)p)->slot0_t; }
 
 void orc_step_update(void* p, const float* x, const float* x0, const float* eps_c, const float* z,
                      const float* x0_new, const float* eps_new, double* x_next, double* out) {

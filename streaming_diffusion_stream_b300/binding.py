@@ -13,11 +13,11 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsds.so")
 
-SDS_ABI_VERSION = 3
+SDS_ABI_VERSION = 4
 SDS_MAX_SLOTS = 8
 SDS_MAX_CHUNK_FRAMES = 8
 SDS_STATE_MAGIC = b"SDSSTAT1"
-SDS_STATE_RECORD_BYTES = 720
+SDS_STATE_RECORD_BYTES = 760
 
 SDS_OK, SDS_ERR_INVALID_ARG, SDS_ERR_OOM, SDS_ERR_CUDA, SDS_ERR_STATE, SDS_ERR_UNSUPPORTED = range(6)
 STATUS_NAMES = {0: "SDS_OK", 1: "SDS_ERR_INVALID_ARG", 2: "SDS_ERR_OOM", 3: "SDS_ERR_CUDA",
@@ -35,7 +35,7 @@ class sds_config(C.Structure):
         ("t_index", _i64 * SDS_MAX_SLOTS)] + [(n, _i64) for n in (
             "num_inference_steps", "num_train_steps", "cfg_type", "slot_elems", "ssf_on",
             "ssf_elems", "max_skip_frame", "motion_on", "frame_elems", "mot_k",
-            "mem_cap_bytes", "attn_ctas", "update_kind")] + [(n, _f64) for n in (
+            "mem_cap_bytes", "attn_ctas", "update_kind", "noise_rate_on")] + [(n, _f64) for n in (
                 "rope_base", "s_th", "beta_start", "beta_end", "gamma", "delta", "ssf_eta",
                 "mot_sigma", "mot_lambda", "s_min", "s_max")]
 
@@ -53,7 +53,8 @@ class sds_stream_state(C.Structure):
                 ("ssf_has_ref", _i64), ("ssf_cos", _f64), ("ssf_p", _f64), ("sink_j", _i64),
                 ("sink_fire", _i64), ("sink_alpha_min", _f64), ("sink_alpha_2", _f64),
                 ("motion_pairs", _i64), ("motion_dhat", _f64), ("noise_rate", _f64),
-                ("motion_d", _f64 * SDS_MAX_CHUNK_FRAMES), ("error_word", _i64)]
+                ("motion_d", _f64 * SDS_MAX_CHUNK_FRAMES), ("error_word", _i64),
+                ("slot0_timestep", _i64)]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -182,6 +183,7 @@ def config_from_workload(w: dict, mem_cap_bytes: int = 0) -> sds_config:
     c.mem_cap_bytes = mem_cap_bytes
     c.attn_ctas = w.get("attn_ctas", 0)
     c.update_kind = w.get("update_kind", 0)
+    c.noise_rate_on = w.get("noise_rate_on", 0)
     c.rope_base, c.s_th = w["rope_base"], w["s_th"]
     c.beta_start, c.beta_end = w["beta_start"], w["beta_end"]
     c.gamma, c.delta, c.ssf_eta = w["gamma"], w["delta"], w["eta"]

@@ -69,6 +69,17 @@ __device__ __forceinline__ void block_sum3(dfloat& a, dfloat& b, dfloat& c, dflo
 __device__ __forceinline__ float4 ld4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+// Schedule coefficients of one slot's update (see StepParams).
+struct SlotCoef {
+  float sa, inv_s1a, s1a, inv_sa;  // sqrt(abar), 1/sqrt(1-abar), sqrt(1-abar), 1/sqrt(abar)
+  float px, pe, sig;               // strided DDPM step to the next slot
+};
+
+__device__ __forceinline__ SlotCoef slot_coef(const StepParams& p, int i) {
+  return SlotCoef{p.c_sa[i], p.c_inv_s1a[i], p.c_s1a[i], p.c_inv_sa[i],
+                  p.c_px[i], p.c_pe[i], p.c_sig[i]};
+}
+
 // eps_cfg = gamma eps_c + delta (1 - gamma) eps_neg with eps_neg the virtual
 // residual (x - sqrt(abar) x0) / sqrt(1 - abar) (cfg_kind 1) or the supplied
 // prediction (cfg_kind 2); eps_c alone without guidance.
@@ -79,26 +90,24 @@ __device__ __forceinline__ float eps_cfg1(float x, float neg, float ec, float sa
 }
 
 __device__ __forceinline__ float4 eps_cfg4(float4 x, float4 neg, float4 ec, const StepParams& p,
-                                           int i) {
+                                           const SlotCoef& k) {
   if (p.cfg_kind == 0) return ec;
-  const float sa = p.c_sa[i], a = p.c_inv_s1a[i];
-  return make_float4(eps_cfg1(x.x, neg.x, ec.x, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
-                     eps_cfg1(x.y, neg.y, ec.y, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
-                     eps_cfg1(x.z, neg.z, ec.z, sa, a, p.c_gamma, p.c_dg, p.cfg_kind),
-                     eps_cfg1(x.w, neg.w, ec.w, sa, a, p.c_gamma, p.c_dg, p.cfg_kind));
+  return make_float4(eps_cfg1(x.x, neg.x, ec.x, k.sa, k.inv_s1a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.y, neg.y, ec.y, k.sa, k.inv_s1a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.z, neg.z, ec.z, k.sa, k.inv_s1a, p.c_gamma, p.c_dg, p.cfg_kind),
+                     eps_cfg1(x.w, neg.w, ec.w, k.sa, k.inv_s1a, p.c_gamma, p.c_dg, p.cfg_kind));
 }
 
 // x0hat = (x - sqrt(1 - abar) eps_cfg) / sqrt(abar)
-__device__ __forceinline__ float4 x0hat4(float4 x, float4 ecfg, const StepParams& p, int i) {
-  const float b = p.c_s1a[i], c = p.c_inv_sa[i];
+__device__ __forceinline__ float4 x0hat4(float4 x, float4 ecfg, const SlotCoef& k) {
+  const float b = k.s1a, c = k.inv_sa;
   return make_float4(__fmaf_rn(-b, ecfg.x, x.x) * c, __fmaf_rn(-b, ecfg.y, x.y) * c,
                      __fmaf_rn(-b, ecfg.z, x.z) * c, __fmaf_rn(-b, ecfg.w, x.w) * c);
 }
 
 // the strided DDPM step: x / sqrt(alpha) - c_pe eps_cfg + sigma z
-__device__ __forceinline__ float4 ddpm4(float4 x, float4 ecfg, float4 z, const StepParams& p,
-                                        int i) {
-  const float cx = p.c_px[i], ce = p.c_pe[i], sg = p.c_sig[i];
+__device__ __forceinline__ float4 ddpm4(float4 x, float4 ecfg, float4 z, const SlotCoef& k) {
+  const float cx = k.px, ce = k.pe, sg = k.sig;
   return make_float4(__fmaf_rn(sg, z.x, __fmaf_rn(-ce, ecfg.x, cx * x.x)),
                      __fmaf_rn(sg, z.y, __fmaf_rn(-ce, ecfg.y, cx * x.y)),
                      __fmaf_rn(sg, z.z, __fmaf_rn(-ce, ecfg.z, cx * x.z)),
@@ -110,40 +119,64 @@ __device__ __forceinline__ float4 noise4(float4 a, float4 b, float ca, float cb)
                      __fmaf_rn(ca, a.z, cb * b.z), __fmaf_rn(ca, a.w, cb * b.w));
 }
 
+// Coefficients of a slot at timestep t from the per-timestep tables.
+__device__ __forceinline__ SlotCoef tab_coef(const StepParams& p, int64_t t) {
+  const float* c = p.coef_tab;
+  const int64_t n = p.n_train;
+  return SlotCoef{__ldg(c + t), __ldg(c + n + t), __ldg(c + 2 * n + t), __ldg(c + 3 * n + t),
+                  __ldg(c + 4 * n + t), __ldg(c + 5 * n + t), __ldg(c + 6 * n + t)};
+}
+
 // One float4 column of every slot: all loads are issued before any store,
 // so the update may run in place (x_next[i] aliasing x[i]) and up to
 // 3N+1 16-byte loads per thread are in flight at once.
 template <int N>
 __device__ void update_block(const StepParams& p, int64_t w) {
   const int64_t s = w / p.nb_u, b = w - s * p.nb_u;
+  SlotCoef k0 = slot_coef(p, 0);
+  float new_sa = p.c_sa[0], new_s1a = p.c_s1a[0];
+  if (p.rate_on) {
+    // the frame in slot 0 sits at the timestep it entered at; the incoming
+    // frame enters at the timestep the previous step derived from its rate
+    const DevState* st = p.state + s;
+    const int64_t t_old = st->slot0_t_buf[p.par], t_new = st->entry_t_buf[p.par];
+    k0 = tab_coef(p, t_old);
+    new_sa = __ldg(p.coef_tab + t_new);
+    new_s1a = __ldg(p.coef_tab + 2 * p.n_train + t_new);
+    if (b == 0 && threadIdx.x == 0) {
+      p.state[s].slot0_t_buf[p.par ^ 1] = t_new;
+      p.state[s].pub.slot0_timestep = t_new;
+    }
+  }
   const int64_t el = b * kUpdBlockElems + threadIdx.x * 4;
   if (el >= p.N_s) return;
   const int64_t e = s * p.N_s + el;
-  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   // second operand of the negative branch: x0 (self-negative) or the
-  // supplied negative prediction; not read without guidance
+  // supplied negative prediction; without guidance x itself (unused), so
+  // that every load is unconditional and all are in flight together
   float4 x[N], neg[N], ec[N], z[N > 1 ? N - 1 : 1];
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     x[i] = ld4(p.x[i] + e);
-    neg[i] = p.cfg_kind == 0 ? zero4 : ld4((p.cfg_kind == 2 ? p.eps_neg[i] : p.x0[i]) + e);
+    neg[i] = ld4((p.cfg_kind == 2 ? p.eps_neg[i] : (p.cfg_kind == 1 ? p.x0[i] : p.x[i])) + e);
     ec[i] = ld4(p.eps_c[i] + e);
     if (i < N - 1) z[i] = ld4(p.z[i] + e);
   }
   const float4 xn = ld4(p.x0_new + e), en = ld4(p.eps_new + e);
 #pragma unroll
   for (int i = N - 1; i >= 0; --i) {
-    const float4 ecfg = eps_cfg4(x[i], neg[i], ec[i], p, i);
-    const float4 xh = x0hat4(x[i], ecfg, p, i);
+    const SlotCoef k = i == 0 ? k0 : slot_coef(p, i);
+    const float4 ecfg = eps_cfg4(x[i], neg[i], ec[i], p, k);
+    const float4 xh = x0hat4(x[i], ecfg, k);
     if (i == N - 1) {
       st4(p.out + e, xh);
     } else if (p.upd_kind == 1) {
-      st4(p.x_next[i + 1] + e, ddpm4(x[i], ecfg, z[i], p, i));
+      st4(p.x_next[i + 1] + e, ddpm4(x[i], ecfg, z[i], k));
     } else {
       st4(p.x_next[i + 1] + e, noise4(xh, z[i], p.c_sa[i + 1], p.c_s1a[i + 1]));
     }
   }
-  st4(p.x_next[0] + e, noise4(xn, en, p.c_sa[0], p.c_s1a[0]));
+  st4(p.x_next[0] + e, noise4(xn, en, new_sa, new_s1a));
 }
 
 // SSF and motion work blocks cover kRedBlockElems elements: 8 float4 per
@@ -307,6 +340,10 @@ __device__ void decide(const StepParams& p, int64_t s, const double* sums) {
     st->mot_count = count;
     st->pub.motion_pairs = pairs;
     st->pub.noise_rate = new_rate;
+    // the next step's incoming frame enters at round(rate (N - 1))
+    int64_t t_entry = (int64_t)floor(new_rate * (double)(p.n_train - 1) + 0.5);
+    t_entry = t_entry < 0 ? 0 : (t_entry > p.n_train - 1 ? p.n_train - 1 : t_entry);
+    st->entry_t_buf[p.par ^ 1] = t_entry;
     st->pub.motion_dhat = dhat;
     st->mot_has_prev = 1;
   }

@@ -2,6 +2,7 @@
 // validation, device buffers, host ring metadata, RoPE and schedule tables,
 // and kernel launches.  No compute happens here; every step of the path runs
 // in the kernels of k_attn.cu, k_ring.cu and k_step.cu.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -29,6 +30,8 @@ struct sds_ctx {
   double* partials = nullptr;
   unsigned int* counters = nullptr;  // [1 + S]
   void* attn_ws = nullptr;           // split-key workspace of the attention kernel
+  float* coef_dev = nullptr;         // per-timestep coefficients (noise-rate application)
+  int64_t step_calls = 0;            // sds_step_update calls (parity of the rate buffers)
   std::vector<void*> allocs;
   // tables
   int rope_seg[3] = {0, 0, 0};
@@ -123,6 +126,8 @@ sds_status validate(const sds_config* c, std::string& why) {
     return bad("cfg_type must be 0 (none), 1 (self-negative) or 2 (supplied negative)");
   if (c->update_kind != 0 && c->update_kind != 1)
     return bad("update_kind must be 0 (re-noise x0hat) or 1 (strided DDPM posterior)");
+  if (c->noise_rate_on != 0 && c->noise_rate_on != 1) return bad("noise_rate_on must be 0 or 1");
+  if (c->noise_rate_on && !c->motion_on) return bad("noise_rate_on needs motion_on");
   if (c->attn_ctas < 0 || c->attn_ctas > kAttnMaxCtas) return bad("attn_ctas must be in [0, 160]");
   if (c->slot_elems < 4 || c->slot_elems % 4 != 0) return bad("slot_elems must be a positive multiple of 4");
   if (c->ssf_on) {
@@ -135,6 +140,13 @@ sds_status validate(const sds_config* c, std::string& why) {
     if (c->mot_k < 1 || c->mot_k > kMaxMotionWindow) return bad("mot_k must be in [1, 64]");
     if (!(c->mot_sigma > 0.0)) return bad("mot_sigma must be > 0");
     if (!(c->s_min <= c->s_max)) return bad("s_min must be <= s_max");
+  }
+  if (c->noise_rate_on && c->update_kind == 1 && c->slots_n > 1) {
+    // the strided DDPM step from slot 0 to slot 1 needs slot 0 at least as
+    // noisy as slot 1 whatever timestep the rate picks (alpha <= 1)
+    const int64_t t_lo = (int64_t)std::floor(c->s_min * (double)(c->num_train_steps - 1) + 0.5);
+    const int64_t t1 = (c->num_train_steps - 1) - c->t_index[1] * (c->num_train_steps / c->num_inference_steps);
+    if (t_lo < t1) return bad("noise_rate_on with update_kind 1 needs round(s_min (N-1)) >= slot 1's timestep");
   }
   return SDS_OK;
 }
@@ -202,7 +214,7 @@ StateLayout state_layout(const sds_config& c, bool with_kv) {
   L.ssf_elems = c.ssf_on ? 2 * S * c.ssf_elems : 0;
   L.mot_elems = c.motion_on ? 2 * S * c.frame_elems : 0;
   L.kv_elems = image ? 0 : S * (c.sink_M + c.ring_R) * c.tokens_L * c.heads_H * c.head_dim;
-  L.meta = 8 * 8;
+  L.meta = 16 * 8;
   L.records = S * (int64_t)sizeof(DevState);
   L.emb = L.emb_elems * 4;
   L.ssf = L.ssf_elems * 4;
@@ -253,10 +265,12 @@ sds_status check_state(const sds_config& c, const void* buf, size_t len, std::st
     return SDS_ERR_STATE;
   }
   const int64_t* meta = reinterpret_cast<const int64_t*>(payload);
-  int64_t m[8];
+  int64_t m[16];
   std::memcpy(m, meta, sizeof m);
+  bool tail_zero = true;
+  for (int i = 9; i < 16; ++i) tail_zero = tail_zero && m[i] == 0;
   if (m[0] < 0 || m[1] < 0 || m[1] > m[0] || m[4] < 0 || m[4] > c.sink_M || m[5] < 0 || m[6] < 0 ||
-      m[7] < 0) {
+      m[7] < 0 || m[8] < 0 || !tail_zero) {
     why = "checkpoint metadata out of range";
     return SDS_ERR_STATE;
   }
@@ -311,7 +325,8 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   const int64_t mot_prev = c.motion_on ? 2 * S * c.frame_elems : 0;
   const int64_t partials = S * nb_s * 3 + S * c.frames_T * nb_m;
   const size_t ws_bytes = attn_ws_bytes((int)c.head_dim);
-  const size_t bytes = (size_t)kv_elems * 2 * 2 + (size_t)emb * 4 + (size_t)tab_entries * 8 +
+  const size_t coef_bytes = c.noise_rate_on ? (size_t)c.num_train_steps * 7 * 4 : 0;
+  const size_t bytes = coef_bytes + (size_t)kv_elems * 2 * 2 + (size_t)emb * 4 + (size_t)tab_entries * 8 +
                        (size_t)ssf_ref * 4 + (size_t)mot_prev * 4 + (size_t)S * sizeof(DevState) +
                        (size_t)partials * 8 + (size_t)(S + 1) * 4 + ws_bytes;
   if (c.mem_cap_bytes > 0 && bytes > (size_t)c.mem_cap_bytes)
@@ -366,6 +381,7 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   ALLOC(ctx->partials, partials * 8);
   ALLOC(ctx->counters, (S + 1) * 4);
   ALLOC(ctx->attn_ws, ws_bytes);
+  ALLOC(ctx->coef_dev, coef_bytes);
 #undef ALLOC
 
   // RoPE table: angle pos * base^(-2i/w) in double, stored as fp32 (cos, sin)
@@ -394,6 +410,12 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
       std::memset(&d, 0, sizeof d);
       d.pub.sink_j = -1;
       d.pub.noise_rate = c.s_min;
+      int64_t te = (int64_t)std::floor(c.s_min * (double)(c.num_train_steps - 1) + 0.5);
+      te = std::min<int64_t>(std::max<int64_t>(te, 0), c.num_train_steps - 1);
+      d.entry_t_buf[0] = d.entry_t_buf[1] = te;
+      const int64_t t0 = (c.num_train_steps - 1) - c.t_index[0] * (c.num_train_steps / c.num_inference_steps);
+      d.slot0_t_buf[0] = d.slot0_t_buf[1] = t0;
+      d.pub.slot0_timestep = t0;
       d.pub.sink_alpha_min = INFINITY;
       d.pub.sink_alpha_2 = INFINITY;
       for (double& v : d.pub.motion_d) v = NAN;
@@ -412,6 +434,32 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
     for (int64_t i = 0; i < c.slots_n; ++i) {
       const int64_t t = (c.num_train_steps - 1) - c.t_index[i] * (c.num_train_steps / c.num_inference_steps);
       ctx->abar_slot[i] = ab[(size_t)t];
+    }
+    if (c.noise_rate_on) {
+      // slot 0's coefficients at every timestep it can sit at; the DDPM rows
+      // step from that timestep to slot 1's
+      const int64_t nt = c.num_train_steps;
+      const double an = c.slots_n > 1 ? ctx->abar_slot[1] : 1.0;
+      std::vector<float> tab((size_t)nt * 7, 0.0f);
+      for (int64_t t = 0; t < nt; ++t) {
+        const double a = ab[(size_t)t];
+        tab[(size_t)t] = (float)std::sqrt(a);
+        tab[(size_t)(nt + t)] = (float)(1.0 / std::sqrt(1.0 - a));
+        tab[(size_t)(2 * nt + t)] = (float)std::sqrt(1.0 - a);
+        tab[(size_t)(3 * nt + t)] = (float)(1.0 / std::sqrt(a));
+        if (c.slots_n > 1) {
+          const double al = a / an;
+          tab[(size_t)(4 * nt + t)] = (float)(1.0 / std::sqrt(al));
+          tab[(size_t)(5 * nt + t)] = (float)((1.0 - al) / (std::sqrt(al) * std::sqrt(1.0 - a)));
+          tab[(size_t)(6 * nt + t)] = (float)std::sqrt((1.0 - an) / (1.0 - a) * (1.0 - al));
+        }
+      }
+      e = cudaMemcpy(ctx->coef_dev, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        free_all(ctx);
+        delete ctx;
+        return fail(nullptr, SDS_ERR_CUDA, "table upload failed: %s", cudaGetErrorString(e));
+      }
     }
   }
   if (!image) {
@@ -665,6 +713,8 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
     if (!okp(io->ssf_frame) || !io->ssf_u)
       return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: ssf_frame must be 16-byte aligned and ssf_u non-NULL");
   }
+  if (c.noise_rate_on && !io->motion_chunk)
+    return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: noise_rate_on needs motion_chunk every step");
   if (io->motion_chunk) {
     if (!c.motion_on) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: motion_chunk given but motion_on == 0");
     if (!okp(io->motion_chunk)) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: motion_chunk must be 16-byte aligned");
@@ -695,6 +745,10 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
   }
   p.cfg_kind = (int32_t)c.cfg_type;
   p.upd_kind = (int32_t)c.update_kind;
+  p.rate_on = (int32_t)c.noise_rate_on;
+  p.par = (int32_t)(ctx->step_calls & 1);
+  p.coef_tab = ctx->coef_dev;
+  p.n_train = c.num_train_steps;
   if (c.cfg_type != 0) {
     p.c_gamma = (float)c.gamma;
     p.c_dg = (float)(c.delta * (1.0 - c.gamma));
@@ -716,6 +770,7 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
   cudaError_t e = launch_step(p, ctx->sm_count, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "step_update launch");
   if (io->motion_chunk) ctx->motion_calls++;
+  ctx->step_calls++;
   return SDS_OK;
 }
 
@@ -760,8 +815,9 @@ sds_status sds_state_export(sds_ctx* ctx, void* buf, size_t* len, int64_t with_k
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "state_export");
   unsigned char* out = static_cast<unsigned char*>(buf) + sizeof(sds_state_header);
-  const int64_t meta[8] = {ctx->F, ctx->o, ctx->p0, ctx->chunk_first,
-                           ctx->sinks_filled, ctx->resets, ctx->chunks, ctx->motion_calls};
+  const int64_t meta[16] = {ctx->F, ctx->o, ctx->p0, ctx->chunk_first,
+                            ctx->sinks_filled, ctx->resets, ctx->chunks, ctx->motion_calls,
+                            ctx->step_calls};
   std::memcpy(out, meta, sizeof meta);
   unsigned char* q = out + L.meta;
   struct Sec {
@@ -805,7 +861,7 @@ sds_status sds_state_import(sds_ctx* ctx, const void* buf, size_t len, sds_strea
   std::memcpy(&h, buf, sizeof h);
   const StateLayout L = state_layout(ctx->cfg, (h.flags & 1) != 0);
   const unsigned char* in = static_cast<const unsigned char*>(buf) + sizeof h;
-  int64_t meta[8];
+  int64_t meta[16];
   std::memcpy(meta, in, sizeof meta);
   const unsigned char* q = in + L.meta;
   struct Sec {
@@ -830,6 +886,7 @@ sds_status sds_state_import(sds_ctx* ctx, const void* buf, size_t len, sds_strea
   ctx->resets = meta[5];
   ctx->chunks = meta[6];
   ctx->motion_calls = meta[7];
+  ctx->step_calls = meta[8];
   return SDS_OK;
 }
 

@@ -21,6 +21,11 @@ struct DevState {
   int64_t mot_head;    // next write position in the circular window
   int64_t mot_has_prev;
   double mot_window[kMaxMotionWindow];
+  // noise-rate application, by update-step parity (a step reads [par] and
+  // writes the next step's [par ^ 1]): the timestep at which the step's
+  // incoming frame enters slot 0, and the timestep of the frame already there
+  int64_t entry_t_buf[2];
+  int64_t slot0_t_buf[2];
 };
 
 static_assert(sizeof(DevState) == SDS_STATE_RECORD_BYTES,
@@ -127,6 +132,14 @@ struct StepParams {
   float c_px[SDS_MAX_SLOTS];       // DDPM: 1 / sqrt(alpha_i)
   float c_pe[SDS_MAX_SLOTS];       // DDPM: (1 - alpha_i) / (sqrt(alpha_i) sqrt(1 - abar_i))
   float c_sig[SDS_MAX_SLOTS];      // DDPM: sigma_i
+  // noise-rate application: slot 0's coefficients come from per-stream
+  // timesteps through the abar table
+  int32_t rate_on, par;
+  // per-timestep coefficient tables [7][n_train]: sqrt(abar), 1/sqrt(1-abar),
+  // sqrt(1-abar), 1/sqrt(abar), and the strided DDPM step to slot 1's
+  // timestep: 1/sqrt(alpha), (1-alpha)/(sqrt(alpha) sqrt(1-abar)), sigma
+  const float* coef_tab;
+  int64_t n_train;
   int32_t n;                       // slots (0: no update segment)
   int64_t N_s;
   // SSF segment

@@ -35,6 +35,7 @@ _BASE = dict(
     beta_end=0.012,
     cfg_type=1,          # 1 = self-negative R-CFG, 2 = supplied negative prediction
     update_kind=0,       # 0 = predict x0 then re-noise, 1 = strided DDPM posterior
+    noise_rate_on=0,     # 1 = the incoming frame enters slot 0 at the motion noise rate
     gamma=1.4,
     delta=1.0,
     s_th=0.9,

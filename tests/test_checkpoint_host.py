@@ -27,17 +27,17 @@ def layout(w, with_kv):
     ssf = 2 * S * w["ssf_E"] if w["ssf"] else 0
     mot = 2 * S * w["N_f"] if w["motion"] else 0
     kv = S * (w["M"] + w["R"]) * w["L"] * w["HD"]
-    sizes = [64, S * B.SDS_STATE_RECORD_BYTES, 4 * emb, 4 * ssf, 4 * mot]
+    sizes = [128, S * B.SDS_STATE_RECORD_BYTES, 4 * emb, 4 * ssf, 4 * mot]
     if with_kv:
         sizes += [2 * kv, 2 * kv]
     return dict(emb=emb, ssf=ssf, mot=mot, kv=kv, payload=sum(sizes))
 
 
-def build(cfg, w, with_kv=True, meta=(12, 4, 3, 11, 1, 2, 12, 12), seed=0):
+def build(cfg, w, with_kv=True, meta=(12, 4, 3, 11, 1, 2, 12, 12, 12), seed=0):
     L = layout(w, with_kv)
     rng = np.random.default_rng(seed)
     payload = bytearray(rng.integers(0, 256, L["payload"], dtype=np.uint8).tobytes())
-    payload[:64] = struct.pack("<8q", *meta)
+    payload[:128] = struct.pack("<16q", *(tuple(meta) + (0,) * (16 - len(meta))))
     h = B.sds_state_header()
     h.magic = B.SDS_STATE_MAGIC
     h.abi_version = B.SDS_ABI_VERSION
@@ -78,7 +78,7 @@ def test_every_corruption_is_rejected(setup):
     w, cfg = setup
     good = build(cfg, w)
     flipped = bytearray(good)
-    flipped[128 + 64 + 5] ^= 0x10                     # one payload bit
+    flipped[128 + 128 + 5] ^= 0x10                    # one payload bit
     expect_reject(cfg, bytes(flipped), "hash")
     bad_magic = b"XDSSTAT1" + good[8:]
     expect_reject(cfg, bad_magic, "magic")
@@ -93,7 +93,9 @@ def test_every_corruption_is_rejected(setup):
     h.devstate_bytes = 712
     expect_reject(cfg, bytes(h) + good[128:], "section sizes")
     # metadata out of range, with a valid hash: more sinks filled than exist
-    expect_reject(cfg, build(cfg, w, meta=(12, 4, 3, 11, 5, 2, 12, 12)), "metadata")
+    expect_reject(cfg, build(cfg, w, meta=(12, 4, 3, 11, 5, 2, 12, 12, 12)), "metadata")
+    # reserved metadata words must be zero
+    expect_reject(cfg, build(cfg, w, meta=(12, 4, 3, 11, 1, 2, 12, 12, 12, 7)), "metadata")
 
 
 def test_null_buffer_is_an_argument_error(setup):

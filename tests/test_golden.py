@@ -2,10 +2,7 @@
 values the implementation's readings derive from them) and the oracle's
 regression values (written by tests/golden/make_golden.py from oracle/)."""
 import json
-import math
 import os
-
-import numpy as np
 
 from oracle import oracle as O
 from streaming_diffusion_stream_b300 import workloads as W

@@ -13,8 +13,6 @@ frame holds and the ring is rebuilt with the oracle's push arithmetic at
 each check.  K/V chunks cycle through a pool of four, so the ring keeps
 changing while the inputs stay on the device.
 """
-import ctypes as C
-
 import numpy as np
 import pytest
 import torch
@@ -40,7 +38,7 @@ def export_kv(ctx, w):
     sh = (w["streams"], (w["M"] + w["R"]) * w["L"], w["H"], w["d"])
     k = np.frombuffer(data, dtype=np.uint16, count=n_kv, offset=off).reshape(sh)
     v = np.frombuffer(data, dtype=np.uint16, count=n_kv, offset=off + 2 * n_kv).reshape(sh)
-    emb_off = 128 + 64 + w["streams"] * B.SDS_STATE_RECORD_BYTES
+    emb_off = 128 + 128 + w["streams"] * B.SDS_STATE_RECORD_BYTES
     emb = np.frombuffer(data, dtype=np.float32, count=h.emb_elems, offset=emb_off)
     return k, v, emb.reshape(w["streams"], w["M"], w["D"])
 

@@ -111,6 +111,9 @@ def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_
                     assert st[s]["ssf_skip"] == oss[s]["skip"], (step, s, st[s], oss[s])
                     assert st[s]["ssf_skip_count"] == oss[s]["skip_count"]
                     stats["skips"] += oss[s]["skip"]
+            if w.get("noise_rate_on"):
+                for s in range(S):
+                    assert st[s]["slot0_timestep"] == o.s[s].slot0_timestep(), (step, s)
             if motion:
                 om_ = o.motion(chunk)
                 for s in range(S):
@@ -155,6 +158,20 @@ def test_guidance_and_update_variants(cfg_type, update_kind, n):
     w = W.get_config("c1_tiny", cfg_type=cfg_type, update_kind=update_kind, n=n,
                      t_index=t_index, steps=4)
     run_sequence(w, 4)
+
+
+@pytest.mark.parametrize("update_kind,streams", [(0, 1), (1, 2)])
+def test_noise_rate_sets_the_incoming_frames_timestep(update_kind, streams):
+    """The motion-aware noise rate chooses the timestep at which each
+    stream's incoming frame enters slot 0 (bursts move the rate around)."""
+    w = W.get_config("c1_tiny", noise_rate_on=1, update_kind=update_kind, streams=streams,
+                     burst_prob=0.4, lat_step=0.3, steps=8)
+    run_sequence(w, 8)
+
+
+def test_c3_full_size_with_noise_rate_application():
+    w = W.get_config("c3_dit1p3b_video", noise_rate_on=1, burst_prob=0.5)
+    run_sequence(w, 4, rows_per_step=8, attend_every=3)
 
 
 def test_c4_full_size_ddpm_update_with_supplied_negative():

@@ -621,3 +621,44 @@ def test_ddpm_adjacent_step_noise_scale_is_beta_tilde():
     ab = O.alpha_bar(w)
     sigma = math.sqrt((1 - ab[t1]) / (1 - ab[t0]) * beta)
     assert np.allclose(a - b, sigma, rtol=1e-10)
+
+
+# --------------------------------------------------------------- noise-rate application
+
+def test_noise_rate_sets_the_entry_timestep_and_the_next_update_uses_it():
+    """With the rate at s_min (no motion yet) the incoming frame enters at
+    round(s_min (N - 1)); next step the frame in slot 0 is treated at that
+    timestep: built from its x0 and true noise at that level, it predicts x0."""
+    w = tiny(n=1, T=1, noise_rate_on=1, cfg_type=0, s_min=0.3, s_max=0.9)
+    st = O.Stream(w)
+    N = w["N_s"]
+    rng = np.random.default_rng(9)
+    x0 = rng.standard_normal(N).astype(np.float32)
+    eps = rng.standard_normal(N).astype(np.float32)
+    t_entry = int(math.floor(0.3 * (w["n_train"] - 1) + 0.5))
+    assert t_entry == 300
+    one = lambda a: a[None, :]
+    xn, _ = st.step_update(one(x0), one(x0), one(eps), np.zeros((0, N), np.float32), x0, eps)
+    assert st.slot0_timestep() == t_entry
+    ab = O.alpha_bar(w)[t_entry]
+    expect = math.sqrt(ab) * x0.astype(np.float64) + math.sqrt(1 - ab) * eps.astype(np.float64)
+    assert np.allclose(xn[0], expect, rtol=1e-12, atol=1e-12)
+    # the frame now in slot 0 (x at t_entry, its noise known) completes to its x0
+    xt = xn[0].astype(np.float32)
+    _, out = st.step_update(one(xt), one(x0), one(eps), np.zeros((0, N), np.float32), x0, eps)
+    assert np.allclose(out, x0, atol=2e-6)
+
+
+def test_noise_rate_follows_motion_into_the_entry_timestep():
+    """A burst that clips the motion to 1 drives the rate toward s_max, and
+    the next incoming frame enters at round(rate (N - 1))."""
+    w = tiny(n=2, T=1, noise_rate_on=1, mot_k=1, sigma=1.0, lam=0.5)
+    st = O.Stream(w)
+    N, Nf = w["N_s"], w["N_f"]
+    z = lambda *sh: np.zeros(sh, np.float32)
+    st.motion(z(1, Nf))
+    st.motion(np.full((1, Nf), 5.0, np.float32))         # d = 5 -> dhat = 1
+    s = st.noise_rate()
+    assert abs(s - (0.3 + 0.5 * (0.9 - 0.3))) < 1e-12    # one EMA step of lambda = 0.5 toward s_max
+    st.step_update(z(2, N), z(2, N), z(2, N), z(1, N), z(N), z(N))
+    assert st.slot0_timestep() == int(math.floor(s * (w["n_train"] - 1) + 0.5))
