@@ -66,6 +66,19 @@ __device__ __forceinline__ void block_sum3(dfloat& a, dfloat& b, dfloat& c, dflo
   __syncthreads();
 }
 
+// The same for one value.
+__device__ __forceinline__ void block_sum1(dfloat& a, dfloat* red) {
+  a = df_warp_sum(a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a = red[0];
+    for (int w = 1; w < kWarps; ++w) a = df_add(a, red[w]);
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ float4 ld4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
@@ -258,7 +271,7 @@ __device__ void motion_block(const StepParams& p, int64_t w, dfloat* red) {
       if (e < p.N_f) st4(p.mot_prev_out + s * p.N_f + e, bv[k]);
     }
   }
-  dfloat sq = df_make(0.f), unused1 = df_make(0.f), unused2 = df_make(0.f);
+  dfloat sq = df_make(0.f);
   if (A) {
 #pragma unroll
     for (int k = 0; k < kRedVec; k += 2) {
@@ -275,85 +288,102 @@ __device__ void motion_block(const StepParams& p, int64_t w, dfloat* red) {
       sq = df_add(sq, df_make(acc));
     }
   }
-  block_sum3(sq, unused1, unused2, red);
+  block_sum1(sq, red);
   if (threadIdx.x == 0) p.partials[p.S * p.nb_s * 3 + (s * p.T + j) * p.nb_m + b] = df_to_double(sq);
 }
 
 constexpr int kFinChunk = 32;  // streams finished per round of the last block
 constexpr int kFinPer = 3 + SDS_MAX_CHUNK_FRAMES;  // sums per stream at most
 
-// The SSF decision and the motion / noise-rate update of stream s from its
-// reduced sums (dot, |I|^2, |R|^2, then one squared difference per pair).
-// The record's fields are read in one batch of independent loads, updated
-// in registers and written back, so the chain of dependent global-memory
-// round trips stays short.
-__device__ void decide(const StepParams& p, int64_t s, const double* sums) {
+// The SSF decision and the motion / noise-rate update of stream s, taken by
+// one warp from the stream's reduced values (dot, |I|^2, |R|^2, then the RMS
+// difference d_j of each pair j).  Every lane reads the record's scalar
+// fields (broadcast loads) and two slots of the old motion window; the slot
+// a lane owns ends with the last of the chunk's d values written to it, so
+// the window max needs no read back of what the warp stores.  The results
+// equal those of appending the present pairs one by one to the ring.
+__device__ void decide(const StepParams& p, int64_t s, const double* vals, int lane) {
   DevState* st = p.state + s;
   if (p.ssf_frame) {
-    const int64_t has_ref = st->pub.ssf_has_ref, count = st->pub.ssf_skip_count;
-    const int64_t cur = st->ssf_cur, evals = st->pub.ssf_evals;
-    const double u = (double)__ldcg(p.ssf_u + s);
-    const double dot = sums[0], ni = sums[1], nr = sums[2];
-    double cosv = 0.0, P = 0.0;
-    int64_t skip = 0;
-    if (has_ref) {
-      cosv = (ni > 0.0 && nr > 0.0) ? dot / sqrt(ni * nr) : 0.0;
-      P = fmin(1.0, fmax(0.0, (cosv - p.eta) / (1.0 - p.eta)));
-      skip = (u < P && count < p.max_skip) ? 1 : 0;
+    if (lane == 0) {
+      const int64_t has_ref = st->pub.ssf_has_ref, count = st->pub.ssf_skip_count;
+      const int64_t cur = st->ssf_cur, evals = st->pub.ssf_evals;
+      const double u = (double)__ldcg(p.ssf_u + s);
+      const double dot = vals[0], ni = vals[1], nr = vals[2];
+      double cosv = 0.0, P = 0.0;
+      int64_t skip = 0;
+      if (has_ref) {
+        cosv = (ni > 0.0 && nr > 0.0) ? dot / sqrt(ni * nr) : 0.0;
+        P = fmin(1.0, fmax(0.0, (cosv - p.eta) / (1.0 - p.eta)));
+        skip = (u < P && count < p.max_skip) ? 1 : 0;
+      }
+      st->pub.ssf_skip_count = skip ? count + 1 : 0;
+      st->ssf_cur = skip ? cur : (cur ^ 1);
+      st->pub.ssf_has_ref = skip ? has_ref : 1;
+      st->pub.ssf_skip = skip;
+      st->pub.ssf_cos = cosv;
+      st->pub.ssf_p = P;
+      st->pub.ssf_evals = evals + 1;
     }
-    st->pub.ssf_skip_count = skip ? count + 1 : 0;
-    st->ssf_cur = skip ? cur : (cur ^ 1);
-    st->pub.ssf_has_ref = skip ? has_ref : 1;
-    st->pub.ssf_skip = skip;
-    st->pub.ssf_cos = cosv;
-    st->pub.ssf_p = P;
-    st->pub.ssf_evals = evals + 1;
-    sums += 3;
+    vals += 3;
   }
   if (p.mot_chunk) {
-    const int64_t has_prev = st->mot_has_prev;
-    int64_t head = st->mot_head, count = st->mot_count, pairs = st->pub.motion_pairs;
+    const int K = (int)p.mot_k, T = (int)p.T;
+    const int has_prev = (int)st->mot_has_prev, head = (int)st->mot_head, count = (int)st->mot_count;
+    const int64_t pairs = st->pub.motion_pairs;
     const double rate = st->pub.noise_rate, dhat_old = st->pub.motion_dhat;
-    const double nan = __longlong_as_double(0x7FF8000000000000ll);  // pair absent
-    for (int64_t j = 0; j < p.T; ++j) {
-      const bool present = (j > 0) || (has_prev != 0);
-      double dv = nan;
-      if (present) {
-        dv = sqrt(sums[j] / (double)p.N_f);
-        st->mot_window[head] = dv;
-        head = (head + 1) % p.mot_k;
-        if (count < p.mot_k) count += 1;
-        pairs += 1;
+    double w_old[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) w_old[h] = (lane + 32 * h < K) ? st->mot_window[lane + 32 * h] : 0.0;
+    const int first = has_prev ? 0 : 1;  // pair 0 is absent on the first chunk
+    const int n_new = T - first;          // d values appended, in pair order
+    const int count_new = min(count + n_new, K);
+    const double nan = __longlong_as_double(0x7FF8000000000000ll);
+    double mx = 0.0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = lane + 32 * h;
+      if (q >= K) continue;
+      const int r = (q - head + K) % K;  // appended value r lands on slot q first
+      double v = w_old[h];
+      if (r < n_new) {
+        v = vals[first + r + K * ((n_new - 1 - r) / K)];  // the last one to land there
+        st->mot_window[q] = v;
       }
-      if (j < SDS_MAX_CHUNK_FRAMES) st->pub.motion_d[j] = dv;
+      if (q < count_new) mx = fmax(mx, v);
     }
-    for (int64_t j = p.T; j < SDS_MAX_CHUNK_FRAMES; ++j) st->pub.motion_d[j] = nan;
-    double new_rate = rate, dhat = dhat_old;
-    if (count > 0) {
-      double mx = 0.0;
-      for (int64_t q = 0; q < count; ++q) mx = fmax(mx, st->mot_window[q]);
-      dhat = fmin(1.0, mx / p.sigma);
-      const double target = p.s_min + (p.s_max - p.s_min) * dhat;
-      new_rate = rate + (1.0 - p.lam) * (target - rate);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane < SDS_MAX_CHUNK_FRAMES)
+      st->pub.motion_d[lane] = (lane >= first && lane < T) ? vals[lane] : nan;
+    if (lane == 0) {
+      double new_rate = rate, dhat = dhat_old;
+      if (count_new > 0) {
+        dhat = fmin(1.0, mx / p.sigma);
+        const double target = p.s_min + (p.s_max - p.s_min) * dhat;
+        new_rate = rate + (1.0 - p.lam) * (target - rate);
+      }
+      st->mot_head = (head + n_new) % K;
+      st->mot_count = count_new;
+      st->pub.motion_pairs = pairs + n_new;
+      st->pub.noise_rate = new_rate;
+      // the next step's incoming frame enters at round(rate (N - 1))
+      int64_t t_entry = (int64_t)floor(new_rate * (double)(p.n_train - 1) + 0.5);
+      t_entry = t_entry < 0 ? 0 : (t_entry > p.n_train - 1 ? p.n_train - 1 : t_entry);
+      st->entry_t_buf[p.par ^ 1] = t_entry;
+      st->pub.motion_dhat = dhat;
+      st->mot_has_prev = 1;
     }
-    st->mot_head = head;
-    st->mot_count = count;
-    st->pub.motion_pairs = pairs;
-    st->pub.noise_rate = new_rate;
-    // the next step's incoming frame enters at round(rate (N - 1))
-    int64_t t_entry = (int64_t)floor(new_rate * (double)(p.n_train - 1) + 0.5);
-    t_entry = t_entry < 0 ? 0 : (t_entry > p.n_train - 1 ? p.n_train - 1 : t_entry);
-    st->entry_t_buf[p.par ^ 1] = t_entry;
-    st->pub.motion_dhat = dhat;
-    st->mot_has_prev = 1;
   }
 }
 
 // Run by the last block: every sum of the launch is reduced by one warp in
 // a fixed order (lane-strided over the partials, then a butterfly, which
-// leaves the same bits in every lane), and one thread per stream takes the
-// stream's decisions.  The three SSF sums of a stream follow one order, so
-// identical frames still give dot == |I|^2 == |R|^2 bitwise.
+// leaves the same bits in every lane); a motion sum becomes the pair's RMS
+// difference in the same warp, so the square roots of a chunk run in
+// parallel.  Then one warp per stream takes the stream's decisions.  The
+// three SSF sums of a stream follow one order, so identical frames still
+// give dot == |I|^2 == |R|^2 bitwise.
 __device__ void finalize(const StepParams& p, double* fin) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_ssf = p.ssf_frame ? 3 : 0;
@@ -377,10 +407,10 @@ __device__ void finalize(const StepParams& p, double* fin) {
       double v = 0.0;
       for (int64_t i = lane; i < n; i += 32) v += __ldcg(base + i * stride);
       v = warp_sum(v);
-      if (lane == 0) fin[k] = v;
+      if (lane == 0) fin[k] = q < n_ssf ? v : sqrt(v / (double)p.N_f);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < ns; i += kStepThreads) decide(p, s0 + i, fin + i * per_s);
+    for (int i = warp; i < ns; i += kWarps) decide(p, s0 + i, fin + i * per_s, lane);
     __syncthreads();
   }
 }
