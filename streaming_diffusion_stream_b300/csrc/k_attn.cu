@@ -22,26 +22,39 @@
 //   warps 4-7  softmax group 1 (tile Q1)
 //   warp  8    TMA producer: K and V tiles through an ST-stage ring, Q per item
 //   warp  9    MMA issuer (one thread): tcgen05.mma into tensor memory
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256) fp32 scores;
-// O0 [256, 256+d), O1 [384, 384+d) fp32 accumulators.  Each group writes its
-// probabilities P as packed bf16 over the first 64 columns of its own S
+//   warp  10   d = 64 only: the second MMA issuer
+// d = 128.  Tensor memory (512 columns): S0 [0,128), S1 [128,256) fp32
+// scores; O0 [256,384), O1 [384,512) fp32 accumulators.  Each group writes
+// its probabilities P as packed bf16 over the first 64 columns of its own S
 // region, and O += P V reads P straight from tensor memory (A operand in
-// TMEM), so P never touches shared memory.  The MMA issuer interleaves
+// TMEM), so P never touches shared memory.  The one issuer interleaves
 //   PV0(g), S0(g+1), PV1(g), S1(g+1), ...
 // so the tensor core works on one group's tile while the other group runs
-// its softmax (ping-pong); the waits for K/V data, which the producer lands
-// several tiles ahead, are taken before the wait for P so they stay off the
-// critical path.  tcgen05 MMAs run in issue order, so S_t(g+1) may
-// overwrite the P_t(g) columns that PV_t(g) reads.
+// its softmax (ping-pong); tcgen05 MMAs from one thread run in issue order,
+// so S_t(g+1) may overwrite the P_t(g) columns that PV_t(g) reads.
+// d = 64.  The tensor work of a tile is half as long, so ping-pong alone
+// leaves the tensor core idle while a group's softmax runs.  P_t gets
+// columns of its own (S0, S1, P0, P1, O0, O1 = 128+128+64+64+64+64), and
+// issuer t serves tile t alone: it issues S_t(g+1) as soon as group t has
+// read S_t(g) into registers (s_free), then PV_t(g) once P_t(g) is written,
+// so the next scores are ready when the softmax finishes the current tile.
+// Group t writes P_t(g) only after PV_t(g-1) has completed; it waits for
+// that halfway through its exponentials, holding the first half of P in
+// registers.  The two groups take turns at the exponentials (E0(g), E1(g),
+// E0(g+1), ...): each then has the MUFU pipe to itself while the other
+// loads its scores and takes its row max.  At an item boundary PV_t(g) is issued before S_t(g+1),
+// because the next item's queries are rotated by the softmax only once it
+// has finished the current item.
+// In both cases the waits for K/V data, which the producer lands several
+// tiles ahead, are taken before the wait for P so they stay off the
+// critical path.
 // The online softmax keeps a running max m per row and rescales O (in
 // tensor memory) only when a tile raises m by more than 8 (log2 units):
 // otherwise probabilities may exceed 1 by up to 2^8, which fp32 sums and bf16
-// P hold without loss.  So after an item's first tile the exponentials are
-// taken against the running max straight away, with the tile max computed
-// alongside on another pipe; the rare tile that raises the max past the
-// threshold is redone against its own max.  Score scaling and row sums use packed f32x2
-// arithmetic and the row max a three-input max, halving their instruction
-// count.  Every wait has a time limit; on expiry the kernel records
+// P hold without loss.  Each tile's row max is taken first (a three-input
+// max); the exponentials go against the running max unless the tile raises
+// it past the threshold.  Score scaling and row sums use packed f32x2
+// arithmetic, halving their instruction count.  Every wait has a time limit; on expiry the kernel records
 // kErrAttnWaitTimeout in the error word of every stream and leaves.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -67,17 +80,18 @@ struct Cfg {
   static constexpr int TILE = NSUB * SUB;  // one 128-row tile of Q, K or V
   static constexpr int ST = (D == 64) ? 4 : 2;  // K/V pipeline stages
   static constexpr int QB = (D == 64) ? 2 : 1;  // Q buffers (double-buffered across items if it fits)
-  // d = 64 leaves 64 spare tensor-memory columns after each O accumulator:
-  // P goes there, S stays intact, and exponentials are taken speculatively
-  // against the running max (a tile that raises it is redone from S).
-  static constexpr bool SPEC = false;
-  // d = 64: an M128 N64 MMA from one issuing thread takes about 50 cycles
-  // against 32 of tensor work, while two threads issuing concurrently reach
-  // the full rate.  So each group's P V product is split: kk-steps 0,2,4,6
-  // by issuer A into O columns [0,64), 1,3,5,7 by issuer B into [64,128);
-  // the epilogue adds the halves.
-  static constexpr bool DUAL = (D == 64);
-  static constexpr int OCOLS = DUAL ? 128 : D;  // tensor-memory columns of one O
+  // d = 64 (EARLY): P_t gets tensor-memory columns of its own, so the
+  // issuer of tile t can start S_t(g+1) as soon as the softmax has read
+  // S_t(g) into registers, and each tile has its own issuing thread (an
+  // M128 N64 MMA from one thread takes about 50 cycles against 32 of tensor
+  // work; two threads issuing concurrently reach the full rate).
+  // Layout S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
+  // O0 [384,448) O1 [448,512).  d = 128 has no spare columns: P overwrites
+  // the first 64 columns of its S and one thread issues every MMA.
+  static constexpr bool EARLY = (D == 64);
+  static constexpr int ISS = EARLY ? 2 : 1;  // MMA-issuing threads
+  static constexpr uint32_t O_COL = EARLY ? 384u : 256u;  // first column of O0
+  static constexpr uint32_t O_STRIDE = EARLY ? 64u : 128u;
   static constexpr int Q = 0;
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
@@ -109,7 +123,8 @@ struct Bars {
   uint64_t* p_full;  // [2]
   uint64_t* o_done;  // [2]
   uint64_t* mma_final;  // [2]: issuer A, issuer B
-  uint64_t* pvb_done;   // [2]: issuer B's half of PV_t has landed
+  uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
+  uint64_t* tok;        // [2]: group t has finished its exponentials of a tile (EARLY)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -130,8 +145,9 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.p_full = r.s_full + 2;
   r.o_done = r.p_full + 2;
   r.mma_final = r.o_done + 2;
-  r.pvb_done = r.mma_final + 2;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(r.pvb_done + 2);
+  r.s_free = r.mma_final + 2;
+  r.tok = r.s_free + 2;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.tok + 2);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   return r;
 }
@@ -147,6 +163,17 @@ __device__ __forceinline__ void key_tile(const AttnParams& p, int nt0, int j, in
 }
 
 __device__ __forceinline__ void fail_wait(const Bars& B) { *B.abort_flag = 1; }
+
+// A wait on the softmax path, where a whole score row is live in registers:
+// a short inline spin, then the bounded wait out of line, so that the
+// timer bookkeeping (and the register saves of the call) stay off the
+// usual path.
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity); }
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < 1024; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity);
+}
 
 // The even division of U units over G CTAs: CTA c owns [lo(c), lo(c+1)).
 struct Split {
@@ -232,22 +259,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_v);
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.q_full + i, 1);
-      mbar_init(B.q_empty + i, 1);
+      mbar_init(B.q_empty + i, C::EARLY ? 2 : 1);
       mbar_init(B.q_ready + 2 * i + 0, 128);
       mbar_init(B.q_ready + 2 * i + 1, 128);
     }
     for (int i = 0; i < C::ST; ++i) {
       mbar_init(B.k_full + i, 1);
       mbar_init(B.v_full + i, 1);
-      mbar_init(B.k_empty + i, 1);
-      mbar_init(B.v_empty + i, C::DUAL ? 2 : 1);
+      mbar_init(B.k_empty + i, C::EARLY ? 2 : 1);
+      mbar_init(B.v_empty + i, C::ISS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.s_full + i, 1);
       mbar_init(B.p_full + i, 128);
-      mbar_init(B.o_done + i, C::DUAL ? 2 : 1);
-      mbar_init(B.pvb_done + i, 1);
+      mbar_init(B.o_done + i, 1);
       mbar_init(B.mma_final + i, 1);
+      mbar_init(B.s_free + i, 128);
+      mbar_init(B.tok + i, 128);
     }
     *B.abort_flag = 0;
     fence_barrier_init();
@@ -312,6 +340,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
         mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u);
     }
+  } else if (C::EARLY && (wid == 9 || wid == 10)) {
+    // ------------------------------------------------------------ MMA issuers (d = 64):
+    // one thread per query tile t, for S_t = Q_t K^T and O_t += P_t V.
+    // S_t(g+1) goes out as soon as the softmax has read S_t(g) (s_free) and
+    // before P_t(g) exists, so the next scores are ready when the softmax
+    // finishes the current tile.
+    if (lane == 0 && active) {
+      const int t = wid - 9;
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
+      const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
+      const uint32_t qlo = (uint32_t)smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t klo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
+      const uint32_t dS = tmem + (uint32_t)(t * 128);
+      const uint32_t aP = tmem + 256u + (uint32_t)(t * 64);
+      const uint32_t dO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE;
+      auto issue_s = [&](int qb, uint32_t st) {
+        const uint32_t a0 = qlo + (uint32_t)(((qb * 2 + t) * C::TILE) >> 4);
+        const uint32_t b0 = klo + st * (uint32_t)(C::TILE >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(((kk >> 2) * SUB + (kk & 3) * 32) >> 4);
+          mma_bf16_ss_w(dS, a0 + off, dhi, b0 + off, dhi, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](uint32_t st, bool acc) {
+        const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4), dhi,
+                        IDESC_O, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      uint32_t g = 0;  // global tile counter
+      int sg = 0;      // segment counter
+      int64_t u = u_lo;
+      {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        ok = mbar_wait(B.q_ready + t, 0) && mbar_wait(B.k_full, 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          mma_commit(B.s_full + t);
+          mma_commit(B.k_empty + 0);
+          if (seg_hi - u == 1) mma_commit(B.q_empty + 0);
+        }
+      }
+      while (ok && u < u_hi) {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        const int n_here = (int)(seg_hi - u);
+        const bool final_seg = seg_hi == u_hi;
+        const int n_next = final_seg ? 0 : (int)(min(u_hi, seg_hi + nkt) - seg_hi);
+        const int qb_n = (sg + 1) % C::QB;
+        const uint32_t qp_n = (uint32_t)((sg + 1) / C::QB) & 1u;
+        for (int i = 0; i < n_here; ++i, ++g) {
+          const uint32_t st = g % C::ST, ph = (g / C::ST) & 1u;
+          const uint32_t st1 = (g + 1) % C::ST, ph1 = ((g + 1) / C::ST) & 1u;
+          const bool boundary = i + 1 == n_here;
+          const bool more = !(boundary && final_seg);
+          const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
+          // S_t(g+1); the next item's queries are rotated by the softmax
+          // only after it has finished this item, which needs PV_t(g), so
+          // at a boundary S_t(g+1) goes after PV_t(g)
+          auto next_s = [&]() -> bool {
+            const int qb1 = boundary ? qb_n : sg % C::QB;
+            if (!mbar_wait(B.k_full + st1, ph1) || !mbar_wait(B.s_free + t, g & 1u) ||
+                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n)))
+              return false;
+            tc_fence_after();
+            issue_s(qb1, st1);
+            mma_commit(B.s_full + t);
+            mma_commit(B.k_empty + st1);
+            if (next_last) mma_commit(B.q_empty + qb1);
+            return true;
+          };
+          if (more && !boundary && !next_s()) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(B.v_full + st, ph) || !mbar_wait(B.p_full + t, g & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(st, i > 0);
+          mma_commit(B.o_done + t);
+          mma_commit(B.v_empty + st);
+          if (more && boundary && !next_s()) {
+            ok = false;
+            break;
+          }
+        }
+        u = seg_hi;
+        ++sg;
+      }
+      if (!ok) fail_wait(B);
+      mma_commit(B.mma_final + t);
+      mbar_wait(B.mma_final + t, 0);
+    }
   } else if (wid == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && active) {
@@ -337,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, uint32_t st, bool acc) {
         const uint32_t dO = tmem + 256u + (uint32_t)(t * 128);
-        const uint32_t aP = C::SPEC ? dO + 64u : tmem + (uint32_t)(t * 128);
+        const uint32_t aP = tmem + (uint32_t)(t * 128);
         const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; kk += (C::DUAL ? 2 : 1))
+        for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4), dhi,
                         IDESC_O, (acc || kk > 0) ? 1u : 0u);
       };
@@ -398,8 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qb1 = boundary ? qb_n : sg % C::QB;
           if (more) {
             // S0(g+1) overwrites P0(g): issuer B's half of PV0(g) must have read it
-            if ((C::DUAL && !mbar_wait(B.pvb_done + 0, g & 1u)) ||
-                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n))) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n)) {
               ok = false;
               break;
             }
@@ -416,8 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 1);
           mma_commit(B.v_empty + st);
           if (more) {
-            if ((C::DUAL && !mbar_wait(B.pvb_done + 1, g & 1u)) ||
-                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n))) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n)) {
               ok = false;
               break;
             }
@@ -436,75 +564,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(B.mma_final + 0);
       mbar_wait(B.mma_final + 0, 0);
     }
-  } else if (wid == 10) {
-    // ------------------------------------------------------------ MMA issuer B (d = 64):
-    // the odd kk-steps of every P V product, into the second half of O
-    if (C::DUAL && lane == 0 && active) {
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
-      const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
-      const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
-      bool ok = true;
-      uint32_t g = 0;
-      int64_t u = u_lo;
-      while (ok && u < u_hi) {
-        const int64_t item = u / nkt;
-        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
-        const int n_here = (int)(seg_hi - u);
-        for (int i = 0; i < n_here; ++i, ++g) {
-          const uint32_t st = g % C::ST, ph = (g / C::ST) & 1u;
-          if (!mbar_wait(B.v_full + st, ph)) {
-            ok = false;
-            break;
-          }
-          const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(B.p_full + t, g & 1u)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t dO = tmem + 256u + (uint32_t)(t * 128) + 64u;
-            const uint32_t aP = tmem + (uint32_t)(t * 128);
-#pragma unroll
-            for (int kk = 1; kk < BN / 16; kk += 2)
-              mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8), b0 + (uint32_t)((kk * 16 * 128) >> 4),
-                            dhi, IDESC_O, (i > 0 || kk > 1) ? 1u : 0u);
-            mma_commit(B.o_done + t);
-            mma_commit(B.pvb_done + t);
-          }
-          if (!ok) break;
-          mma_commit(B.v_empty + st);
-        }
-        u = seg_hi;
-      }
-      if (!ok) fail_wait(B);
-      mma_commit(B.mma_final + 1);
-      mbar_wait(B.mma_final + 1, 0);
-    }
   } else if (wid < 8 && active) {
     // ------------------------------------------------------------ softmax groups
     const int t = wid >> 2;   // query tile of this group
     const int r = tid & 127;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((wid & 3) * 32) << 16;
     const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_base;
-    const uint32_t tO = tmem + 256u + (uint32_t)(t * 128) + lane_base;
-    const uint32_t tP = C::SPEC ? tO + 64u : tS;  // packed bf16 probabilities
-    // 32 columns of this row's O (the sum of the two halves for d = 64)
+    const uint32_t tO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE + lane_base;
+    // packed bf16 probabilities: own columns (EARLY) or over the scores
+    const uint32_t tP = C::EARLY ? tmem + 256u + (uint32_t)(t * 64) + lane_base : tS;
+    // 32 columns of this row's O
     auto load_o = [&](int c, float(&tmp)[32]) {
       tmem_ld32(tO + (uint32_t)(c * 32), tmp);
-      if (C::DUAL) {
-        float t2[32];
-        tmem_ld32(tO + 64u + (uint32_t)(c * 32), t2);
-        tmem_wait_ld();
-        reg_fence32(tmp);
-        reg_fence32(t2);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) tmp[q] += t2[q];
-      } else {
-        tmem_wait_ld();
-        reg_fence32(tmp);
-      }
+      tmem_wait_ld();
+      reg_fence32(tmp);
     };
     const float sc = p.scale_log2;
     const float2 sc2 = make_float2(sc, sc);
@@ -555,6 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
+        if (C::EARLY) {
+          // the scores are in registers: the issuer may overwrite them
+          tc_fence_before();
+          mbar_arrive(B.s_free + t);
+        }
         int key0, nvalid;
         key_tile(p, nt0, kt, key0, nvalid);
         if (nvalid < BN) {
@@ -562,34 +640,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN; ++c)
             sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
         }
-        // P = exp2(s*sc - m) as packed bf16 over the first 64 columns of S;
-        // returns the row sum of this tile's probabilities.  With WITH_MAX
-        // the tile's raw score max is accumulated into tmax on the way.
-        auto exp_pass = [&](float m, auto with_max, float& tmax) -> float {
-          constexpr bool WM = decltype(with_max)::value;
+        // P = exp2(s*sc - m) as packed bf16, stored as it is made over the
+        // first 64 columns of S (or, EARLY, P_t's own columns); returns the
+        // row sum of this tile's probabilities.
+        // EARLY: P_t(g) may overwrite P_t(g-1) only once PV_t(g-1) has read it
+        auto p_free = [&]() -> bool {
+          if (!C::EARLY || g == 0) return true;
+          if (!wait_spin(B.o_done + t, (uint32_t)(g - 1) & 1u)) return false;
+          tc_fence_after();
+          return true;
+        };
+        uint32_t pk[4][16];
+        bool pwait_ok = true;
+        auto exp_pass = [&](float m) -> float {
           const float2 nm2 = make_float2(-m, -m);
           float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int part = 0; part < 4; ++part) {
-            uint32_t pk[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const float a0 = sv[part][2 * q], a1 = sv[part][2 * q + 1];
-              if (WM) mx[q & 3] = fmax3(mx[q & 3], a0, a1);
               const float2 x = __ffma2_rn(make_float2(a0, a1), sc2, nm2);
               const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
               rs[q & 3] = __fadd2_rn(rs[q & 3], make_float2(e0, e1));
-              pk[q] = pack_bf16x2(e0, e1);
+              pk[part][q] = pack_bf16x2(e0, e1);
             }
-            tmem_st16u(tP + (uint32_t)(part * 16), pk);
+            if (!C::EARLY || part >= 2) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
+            if (C::EARLY && part == 1) {
+              pwait_ok = p_free();
+              tmem_st16u(tP, pk[0]);
+              tmem_st16u(tP + 16u, pk[1]);
+            }
           }
-          if (WM) tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float2 s01 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
           return s01.x + s01.y;
         };
-        float alpha = 1.f, m_new, lsum, tmax = -INFINITY;
+        float alpha = 1.f, m_new, lsum;
+        // EARLY: the two groups take turns at the exponentials (E0(g), E1(g),
+        // E0(g+1), ...), so each runs alone on the MUFU pipe while the other
+        // loads scores and takes its row max
+        auto take_turn = [&]() -> bool {
+          if (!C::EARLY) return true;
+          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u);
+          return wait_spin(B.tok + 0, (uint32_t)g & 1u);
+        };
+        auto give_turn = [&]() {
+          if (C::EARLY) mbar_arrive(B.tok + t);
+        };
         auto row_max = [&]() {
           float mx[4];
 #pragma unroll
@@ -605,40 +703,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kt == k0) {
           // first tile of the item: its own max first
           m_new = row_max();
-          lsum = exp_pass(m_new, std::false_type{}, tmax);
-        } else if (C::SPEC) {
-          // against the running max, checking the tile max on the way
-          m_new = m_run;
-          lsum = exp_pass(m_run, std::true_type{}, tmax);
-          const float mt = tmax * sc;
-          const bool need = mt > m_run + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            if (need) {
-              m_new = mt;
-              alpha = fast_exp2(m_run - m_new);
-            }
-            // redo from S, which is still in tensor memory
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
-            if (nvalid < BN) {
-#pragma unroll
-              for (int c = 0; c < BN; ++c)
-                sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
-            }
-            tmem_wait_st();
-            lsum = exp_pass(m_new, std::false_type{}, tmax);
-            rescale = true;
+          if (!take_turn()) {
+            ok = false;
+            break;
           }
+          lsum = exp_pass(m_new);
+          give_turn();
         } else {
           const float mt = row_max();
           const bool need = mt > m_run + kRescaleThreshold;
           m_new = need ? mt : m_run;
           alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-          lsum = exp_pass(m_new, std::false_type{}, tmax);
+          if (!take_turn()) {
+            ok = false;
+            break;
+          }
+          lsum = exp_pass(m_new);
+          give_turn();
           rescale = __any_sync(0xffffffffu, need);
+        }
+        if (!pwait_ok) {
+          ok = false;
+          break;
         }
         if (rescale) {
           // O may be rescaled only once the previous PV into it has landed
@@ -648,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < C::OCOLS / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             float tmp[32];
             tmem_ld32(tO + (uint32_t)(c * 32), tmp);
             tmem_wait_ld();
