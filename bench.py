@@ -376,7 +376,6 @@ def run_ours(args):
         evi = {n: (ev[n][0][i], ev[n][1][i]) for n in names}
         run.step(run.sets[(warm + i) % run.n_sets], evi)
     t_end.record(stream)
-    wall_enq = time.time()  # host enqueue done: the GPU is the bottleneck if this is well ahead
     torch.cuda.synchronize()
     wall1 = time.time()
     barrier(world)
@@ -436,7 +435,6 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": run.launches_per_step() * steps, "clocks": clocks,
-        "host_enqueue_ms_per_step": round((wall_enq - wall0) * 1e3 / steps, 4),
     }
     run.close()
     if rank == 0:
