@@ -130,7 +130,8 @@ __device__ void copy_frame(const SinkParams& p, int64_t s, int64_t src_row0, int
 __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) {
   __shared__ dfloat red[kRingThreads / 32];
   __shared__ double bcast;
-  __shared__ int last;
+  __shared__ int64_t dec_j;
+  __shared__ int last, dec_fire;
   const int64_t s = blockIdx.y;
   const float* h = p.h + s * p.D;
   DevState* st = p.state + s;
@@ -169,16 +170,26 @@ __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) 
     }
     const double dot = block_sum_df(dot_t, red, &bcast);
     const double en = block_sum_df(en_t, red, &bcast);
-    const double a = (hn > 0.0 && en > 0.0) ? dot / sqrt(hn * en) : 0.0;
-    if (a < amin) {
-      a2 = amin;
-      amin = a;
-      jstar = j;
-    } else if (a < a2) {
-      a2 = a;
+    if (threadIdx.x == 0) {
+      // fp64 divide and square root take hundreds of cycles per warp on
+      // this part's narrow fp64 pipe: one thread takes the decision
+      const double a = (hn > 0.0 && en > 0.0) ? dot / sqrt(hn * en) : 0.0;
+      if (a < amin) {
+        a2 = amin;
+        amin = a;
+        jstar = j;
+      } else if (a < a2) {
+        a2 = a;
+      }
     }
   }
-  const bool fire = amin < p.s_th;
+  if (threadIdx.x == 0) {
+    dec_j = jstar;
+    dec_fire = amin < p.s_th ? 1 : 0;
+  }
+  __syncthreads();
+  jstar = dec_j;
+  const bool fire = dec_fire != 0;
   if (fire) {
     const int64_t slot = p.chunk_first % p.R;
     copy_frame(p, s, (p.M + slot) * p.L, jstar * p.L);
