@@ -117,10 +117,18 @@ def load_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's sources with // comments and blank
+    lines removed, so that a comment edit does not orphan an ncu capture."""
     import hashlib
     h = hashlib.sha256()
     for f in ("k_attn.cu", "ptx.cuh", "rope.cuh"):
-        h.update(open(os.path.join(ROOT, "streaming_diffusion_stream_b300", "csrc", f), "rb").read())
+        lines = []
+        for line in open(os.path.join(ROOT, "streaming_diffusion_stream_b300", "csrc", f)):
+            i = line.find("//")
+            code = (line[:i] if i >= 0 else line).rstrip()
+            if code.strip():
+                lines.append(code)
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 

@@ -122,7 +122,7 @@ struct Bars {
   uint64_t* s_full;  // [2]
   uint64_t* p_full;  // [2]
   uint64_t* o_done;  // [2]
-  uint64_t* mma_final;  // [2]: issuer A, issuer B
+  uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
   uint64_t* tok;        // [2]: group t has finished its exponentials of a tile (EARLY)
   uint32_t* tmem_slot;
@@ -527,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 0);
           const int qb1 = boundary ? qb_n : sg % C::QB;
           if (more) {
-            // S0(g+1) overwrites P0(g): issuer B's half of PV0(g) must have read it
             if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n)) {
               ok = false;
               break;
