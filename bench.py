@@ -56,6 +56,10 @@ def parse():
                     help="0 predict x0 and re-noise, 1 strided DDPM posterior")
     ap.add_argument("--noise-rate-on", action="store_true",
                     help="the incoming frame enters slot 0 at the motion noise rate")
+    ap.add_argument("--eps-c-bf16", action="store_true",
+                    help="the noise predictions eps_c arrive as bf16")
+    ap.add_argument("--txt2img", action="store_true",
+                    help="no input image: the incoming frame is the noise draw (cfg_type 0 unless given)")
     ap.add_argument("--sweep-streams", type=int, default=0,
                     help="print one line per stream count B = 1..N (same workload, one GPU)")
     return ap.parse_args()
@@ -73,6 +77,11 @@ def workload(args, rank: int = 0) -> dict:
         over["update_kind"] = args.update_kind
     if getattr(args, "noise_rate_on", False):
         over["noise_rate_on"] = 1
+    if getattr(args, "eps_c_bf16", False):
+        over["eps_c_bf16"] = 1
+    if getattr(args, "txt2img", False):
+        over["txt2img"] = 1
+        over.setdefault("cfg_type", 0)
     w = W.get_config(args.workload, **over)
     w["seed"] = w["seed"] + 1000 * rank
     return w
@@ -94,6 +103,10 @@ def step_bytes(w: dict, with_ssf: bool, with_motion: bool) -> float:
     # x0_new, eps_new read | x_next (n), out written
     per_slot = 5 if w.get("cfg_type", 1) != 0 else 4
     b = 4.0 * S * w["N_s"] * (per_slot * n + 2)
+    if w.get("eps_c_bf16"):
+        b -= 2.0 * S * w["N_s"] * n       # eps_c read as 2-byte values
+    if w.get("txt2img"):
+        b -= 4.0 * S * w["N_s"]           # no x0_new
     if with_ssf:
         b += 4.0 * S * w["ssf_E"] * 3     # frame, reference | reference copy
     if with_motion:
@@ -253,6 +266,8 @@ class Runner:
         k, v = W.gen_kv(w, i)
         d = dict(q=W.gen_q(w, i), k=k, v=v)
         lat = W.gen_latents(w, i)
+        if w.get("eps_c_bf16"):
+            lat["eps_c"] = W.to_bf16_bits(lat["eps_c"])
         d.update(lat)
         if w["ssf"]:
             d["frame"] = W.FrameWalk(dict(w, seed=w["seed"] + 7919 * (i + 1))).next()
@@ -280,7 +295,8 @@ class Runner:
         return self.B.make_step_io([s["x"][i] for i in range(n)], [s["x0"][i] for i in range(n)],
                                    [s["eps_c"][i] for i in range(n)],
                                    [s["z"][i] for i in range(n - 1)], self.x_next, self.out,
-                                   s["x0_new"], s["eps_new"], s.get("frame"), s.get("u"),
+                                   None if self.w.get("txt2img") else s["x0_new"], s["eps_new"],
+                                   s.get("frame"), s.get("u"),
                                    s.get("chunk"), en)
 
     def step(self, s: dict, ev=None):

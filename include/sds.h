@@ -61,7 +61,7 @@ extern "C" {
 #define SDS_API
 #endif
 
-#define SDS_ABI_VERSION 4
+#define SDS_ABI_VERSION 5
 #define SDS_MAX_SLOTS 8
 #define SDS_MAX_CHUNK_FRAMES 8
 
@@ -114,6 +114,13 @@ typedef enum {
  * t_s (needs motion_on; sds_stream_state.slot0_timestep reports t_s).
  * With update_kind 1, round(s_min * (num_train_steps - 1)) must not fall
  * below slot 1's timestep (else SDS_ERR_INVALID_ARG).
+ * eps_c_bf16: 1 = the eps_c[i] buffers hold bf16 values (the usual output
+ * dtype of the noise-prediction network); the update widens them exactly
+ * to fp32.  0 = fp32.
+ * txt2img: 1 = no input image ([SDO] txt2img): the incoming frame is the
+ * noise draw eps_new itself (the initial latent), x0_new is not read and
+ * may be NULL; cfg_type must be 0 or 2 (self-negative R-CFG needs x0) and
+ * noise_rate_on 0.
  * update_kind: 0 = predict x0 and re-noise it to the next slot's level;
  * 1 = the DDPM ancestral step ([BLOG] section 7) taken between the slot's
  * timestep t and the next slot's t', with alpha = abar_t / abar_t' and
@@ -147,6 +154,8 @@ typedef struct {
   int64_t attn_ctas;
   int64_t update_kind;
   int64_t noise_rate_on;
+  int64_t eps_c_bf16;
+  int64_t txt2img;
   double rope_base, s_th, beta_start, beta_end, gamma, delta, ssf_eta;
   double mot_sigma, mot_lambda, s_min, s_max;
 } sds_config;
@@ -156,14 +165,16 @@ typedef struct {
  * array is fp32, device, [S][slot_elems] (stream-major) unless stated.
  *   x[i]      slot i's current latent x_{t_i}, i < n
  *   x0[i]     slot i's own input-frame latent (the R-CFG x0)
- *   eps_c[i]  the model's conditional noise prediction for slot i
+ *   eps_c[i]  the model's conditional noise prediction for slot i (bf16
+ *             values when eps_c_bf16; 16-byte aligned either way)
  *   z[i]      ancestral noise that re-noises slot i's prediction to slot
  *             i+1's level, i < n-1
  *   x_next[i] next step's latents: x_next[0] is the incoming frame noised to
  *             slot 0's level; x_next[i+1] comes from slot i.  x_next[i] may
  *             alias x[i] (in-place update is safe).
  *   out       the completed frame: slot n-1's predicted x0
- *   x0_new, eps_new  the incoming frame's latent and its noise
+ *   x0_new, eps_new  the incoming frame's latent and its noise (txt2img:
+ *             x0_new unused, the incoming frame is eps_new)
  *   ssf_frame [S][ssf_elems] or NULL: run the similarity filter on this
  *             frame in the same pass; ssf_u [S] uniform draws in [0,1)
  *   motion_chunk [S][frames_T][frame_elems] or NULL: update the motion

@@ -240,17 +240,19 @@ class Stream:
 
     def step_update(self, x, x0, eps_c, z, x0_new, eps_new, eps_neg=None):
         """Slot arrays [n][N_s] (z: [n-1][N_s]) for this stream; eps_neg [n][N_s]
-        for cfg_type 2; returns (x_next, out)."""
+        for cfg_type 2; x0_new None for txt2img; returns (x_next, out)."""
         w = self.w
         n, N = w["n"], w["N_s"]
         f = lambda a: np.ascontiguousarray(a, dtype=np.float32)
-        x, x0, eps_c, x0_new, eps_new = map(f, (x, x0, eps_c, x0_new, eps_new))
+        x, x0, eps_c, eps_new = map(f, (x, x0, eps_c, eps_new))
+        x0_new = f(x0_new) if x0_new is not None else None  # None: txt2img
         z = f(z) if n > 1 else np.zeros((1, N), dtype=np.float32)
         en = f(eps_neg) if eps_neg is not None else np.zeros((n, N), dtype=np.float32)
         xn = np.zeros((n, N), dtype=np.float64)
         out = np.zeros(N, dtype=np.float64)
-        lib().orc_step_update2(self.h, _p(x), _p(x0), _p(eps_c), _p(z), _p(en), _p(x0_new),
-                               _p(eps_new), _p(xn), _p(out))
+        lib().orc_step_update2(self.h, _p(x), _p(x0), _p(eps_c), _p(z), _p(en),
+                               _p(x0_new) if x0_new is not None else None, _p(eps_new), _p(xn),
+                               _p(out))
         return xn, out
 
     def ssf(self, frame: np.ndarray, u: float) -> dict:

@@ -615,9 +615,12 @@ void orc_step_update2(void* p, const float* x, const float* x0, const float* eps
       }
     }
   }
+  // the incoming frame noised to its entry level; with no input image
+  // (txt2img, x0_new absent) the incoming latent is the noise draw itself
   double ab0 = s->abar[(size_t)t_new];
   for (long long e = 0; e < N; ++e)
-    x_next[e] = std::sqrt(ab0) * (double)x0_new[e] + std::sqrt(1.0 - ab0) * (double)eps_new[e];
+    x_next[e] = x0_new ? std::sqrt(ab0) * (double)x0_new[e] + std::sqrt(1.0 - ab0) * (double)eps_new[e]
+                       : (double)eps_new[e];
   s->slot0_t = t_new;
 }
 

@@ -13,7 +13,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsds.so")
 
-SDS_ABI_VERSION = 4
+SDS_ABI_VERSION = 5
 SDS_MAX_SLOTS = 8
 SDS_MAX_CHUNK_FRAMES = 8
 SDS_STATE_MAGIC = b"SDSSTAT1"
@@ -35,7 +35,8 @@ class sds_config(C.Structure):
         ("t_index", _i64 * SDS_MAX_SLOTS)] + [(n, _i64) for n in (
             "num_inference_steps", "num_train_steps", "cfg_type", "slot_elems", "ssf_on",
             "ssf_elems", "max_skip_frame", "motion_on", "frame_elems", "mot_k",
-            "mem_cap_bytes", "attn_ctas", "update_kind", "noise_rate_on")] + [(n, _f64) for n in (
+            "mem_cap_bytes", "attn_ctas", "update_kind", "noise_rate_on", "eps_c_bf16",
+            "txt2img")] + [(n, _f64) for n in (
                 "rope_base", "s_th", "beta_start", "beta_end", "gamma", "delta", "ssf_eta",
                 "mot_sigma", "mot_lambda", "s_min", "s_max")]
 
@@ -184,6 +185,8 @@ def config_from_workload(w: dict, mem_cap_bytes: int = 0) -> sds_config:
     c.attn_ctas = w.get("attn_ctas", 0)
     c.update_kind = w.get("update_kind", 0)
     c.noise_rate_on = w.get("noise_rate_on", 0)
+    c.eps_c_bf16 = w.get("eps_c_bf16", 0)
+    c.txt2img = w.get("txt2img", 0)
     c.rope_base, c.s_th = w["rope_base"], w["s_th"]
     c.beta_start, c.beta_end = w["beta_start"], w["beta_end"]
     c.gamma, c.delta, c.ssf_eta = w["gamma"], w["delta"], w["eta"]

@@ -82,6 +82,13 @@ __device__ __forceinline__ void block_sum1(dfloat& a, dfloat* red) {
 __device__ __forceinline__ float4 ld4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+// Four bf16 values at element offset e of a bf16 array, widened exactly.
+__device__ __forceinline__ float4 ld4_bf16(const float* base, int64_t e) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + e));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
 // Schedule coefficients of one slot's update (see StepParams).
 struct SlotCoef {
   float sa, inv_s1a, s1a, inv_sa;  // sqrt(abar), 1/sqrt(1-abar), sqrt(1-abar), 1/sqrt(abar)
@@ -172,10 +179,12 @@ __device__ void update_block(const StepParams& p, int64_t w) {
   for (int i = 0; i < N; ++i) {
     x[i] = ld4(p.x[i] + e);
     neg[i] = ld4((p.cfg_kind == 2 ? p.eps_neg[i] : (p.cfg_kind == 1 ? p.x0[i] : p.x[i])) + e);
-    ec[i] = ld4(p.eps_c[i] + e);
+    ec[i] = p.ec_bf16 ? ld4_bf16(p.eps_c[i], e) : ld4(p.eps_c[i] + e);
     if (i < N - 1) z[i] = ld4(p.z[i] + e);
   }
-  const float4 xn = ld4(p.x0_new + e), en = ld4(p.eps_new + e);
+  // txt2img: no input frame; the incoming latent is the noise draw itself
+  const float4 en = ld4(p.eps_new + e);
+  const float4 xn = p.txt2img ? en : ld4(p.x0_new + e);
 #pragma unroll
   for (int i = N - 1; i >= 0; --i) {
     const SlotCoef k = i == 0 ? k0 : slot_coef(p, i);
@@ -189,7 +198,7 @@ __device__ void update_block(const StepParams& p, int64_t w) {
       st4(p.x_next[i + 1] + e, noise4(xh, z[i], p.c_sa[i + 1], p.c_s1a[i + 1]));
     }
   }
-  st4(p.x_next[0] + e, noise4(xn, en, new_sa, new_s1a));
+  st4(p.x_next[0] + e, p.txt2img ? en : noise4(xn, en, new_sa, new_s1a));
 }
 
 // SSF and motion work blocks cover kRedBlockElems elements: 8 float4 per

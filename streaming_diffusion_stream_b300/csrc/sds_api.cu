@@ -128,6 +128,10 @@ sds_status validate(const sds_config* c, std::string& why) {
     return bad("update_kind must be 0 (re-noise x0hat) or 1 (strided DDPM posterior)");
   if (c->noise_rate_on != 0 && c->noise_rate_on != 1) return bad("noise_rate_on must be 0 or 1");
   if (c->noise_rate_on && !c->motion_on) return bad("noise_rate_on needs motion_on");
+  if (c->eps_c_bf16 != 0 && c->eps_c_bf16 != 1) return bad("eps_c_bf16 must be 0 or 1");
+  if (c->txt2img != 0 && c->txt2img != 1) return bad("txt2img must be 0 or 1");
+  if (c->txt2img && c->cfg_type == 1) return bad("txt2img has no x0: cfg_type must be 0 or 2");
+  if (c->txt2img && c->noise_rate_on) return bad("txt2img has no input frame to noise: noise_rate_on must be 0");
   if (c->attn_ctas < 0 || c->attn_ctas > kAttnMaxCtas) return bad("attn_ctas must be in [0, 160]");
   if (c->slot_elems < 4 || c->slot_elems % 4 != 0) return bad("slot_elems must be a positive multiple of 4");
   if (c->ssf_on) {
@@ -706,8 +710,9 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
     if (i < n - 1 && !okp(io->z[i]))
       return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: z[%d] must be non-NULL and 16-byte aligned", i);
   }
-  if (!okp(io->out) || !okp(io->x0_new) || !okp(io->eps_new))
-    return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: out, x0_new, eps_new must be non-NULL and 16-byte aligned");
+  if (!okp(io->out) || (!c.txt2img && !okp(io->x0_new)) || !okp(io->eps_new))
+    return fail(ctx, SDS_ERR_INVALID_ARG,
+                "step_update: out, eps_new and (unless txt2img) x0_new must be non-NULL and 16-byte aligned");
   if (io->ssf_frame) {
     if (!c.ssf_on) return fail(ctx, SDS_ERR_INVALID_ARG, "step_update: ssf_frame given but ssf_on == 0");
     if (!okp(io->ssf_frame) || !io->ssf_u)
@@ -746,6 +751,8 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
   p.cfg_kind = (int32_t)c.cfg_type;
   p.upd_kind = (int32_t)c.update_kind;
   p.rate_on = (int32_t)c.noise_rate_on;
+  p.ec_bf16 = (int32_t)c.eps_c_bf16;
+  p.txt2img = (int32_t)c.txt2img;
   p.par = (int32_t)(ctx->step_calls & 1);
   p.coef_tab = ctx->coef_dev;
   p.n_train = c.num_train_steps;
@@ -757,7 +764,7 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
     p.c_dg = 0.0f;
   }
   p.out = io->out;
-  p.x0_new = io->x0_new;
+  p.x0_new = c.txt2img ? nullptr : io->x0_new;
   p.eps_new = io->eps_new;
   p.ssf_frame = io->ssf_frame;
   p.ssf_u = io->ssf_u;

@@ -135,6 +135,8 @@ struct StepParams {
   // noise-rate application: slot 0's coefficients come from per-stream
   // timesteps through the abar table
   int32_t rate_on, par;
+  int32_t ec_bf16;   // eps_c[i] hold bf16 values
+  int32_t txt2img;   // the incoming frame is eps_new itself
   // per-timestep coefficient tables [7][n_train]: sqrt(abar), 1/sqrt(1-abar),
   // sqrt(1-abar), 1/sqrt(abar), and the strided DDPM step to slot 1's
   // timestep: 1/sqrt(alpha), (1-alpha)/(sqrt(alpha) sqrt(1-abar)), sigma

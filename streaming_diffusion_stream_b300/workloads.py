@@ -36,6 +36,8 @@ _BASE = dict(
     cfg_type=1,          # 1 = self-negative R-CFG, 2 = supplied negative prediction
     update_kind=0,       # 0 = predict x0 then re-noise, 1 = strided DDPM posterior
     noise_rate_on=0,     # 1 = the incoming frame enters slot 0 at the motion noise rate
+    eps_c_bf16=0,        # 1 = the noise predictions eps_c arrive as bf16
+    txt2img=0,           # 1 = no input image: the incoming frame is the noise draw itself
     gamma=1.4,
     delta=1.0,
     s_th=0.9,

@@ -126,6 +126,8 @@ class GpuPipe:
     def step(self, lat: dict, ssf_frame=None, u=None, motion_chunk=None):
         n = self.w["n"]
         dev = {k: f32_dev(v) for k, v in lat.items() if k not in ("z", "eps_neg")}
+        if self.w.get("eps_c_bf16"):  # the predictions as bf16 tensors
+            dev["eps_c"] = [bf16_dev(W.to_bf16_bits(lat["eps_c"][i])) for i in range(n)]
         z = [f32_dev(lat["z"][i]) for i in range(n - 1)]
         en = [f32_dev(lat["eps_neg"][i]) for i in range(n)] if "eps_neg" in lat else None
         sf = f32_dev(ssf_frame) if ssf_frame is not None else None
@@ -133,7 +135,8 @@ class GpuPipe:
         mc = f32_dev(motion_chunk) if motion_chunk is not None else None
         io = B.make_step_io([dev["x"][i] for i in range(n)], [dev["x0"][i] for i in range(n)],
                             [dev["eps_c"][i] for i in range(n)], z, self.x_next, self.out,
-                            dev["x0_new"], dev["eps_new"], sf, ut, mc, en)
+                            None if self.w.get("txt2img") else dev["x0_new"], dev["eps_new"], sf,
+                            ut, mc, en)
         B.sds_step_update(self.ctx, io)
         torch.cuda.synchronize()
         xn = np.stack([t.cpu().numpy() for t in self.x_next])  # [n][S][N]
@@ -184,12 +187,16 @@ class OraclePipe:
 
     def step(self, lat: dict):
         n = self.w["n"]
+        ec = lat["eps_c"]
+        if self.w.get("eps_c_bf16"):  # the values the bf16 tensors hold
+            ec = W.bf16_bits_to_f32(W.to_bf16_bits(ec))
         res = []
         for i, s in enumerate(self.s):
             z = lat["z"][:, i] if n > 1 else None
             en = lat["eps_neg"][:, i] if "eps_neg" in lat else None
-            res.append(s.step_update(lat["x"][:, i], lat["x0"][:, i], lat["eps_c"][:, i], z,
-                                     lat["x0_new"][i], lat["eps_new"][i], eps_neg=en))
+            x0n = None if self.w.get("txt2img") else lat["x0_new"][i]
+            res.append(s.step_update(lat["x"][:, i], lat["x0"][:, i], ec[:, i], z, x0n,
+                                     lat["eps_new"][i], eps_neg=en))
         return res
 
     def ssf(self, frame, u):

@@ -86,6 +86,9 @@ def _create_status(cfg):
     ("mot_k", 65, "mot_k"),
     ("cfg_type", 3, "cfg_type"),
     ("update_kind", 2, "update_kind"),
+    ("eps_c_bf16", 2, "eps_c_bf16"),
+    ("txt2img", 2, "txt2img"),
+    ("txt2img", 1, "cfg_type must be 0 or 2"),  # c1 runs self-negative R-CFG
     ("streams", 0, "streams"),
 ])
 def test_invalid_configs_are_rejected_on_the_host(field, value, msg):
@@ -151,3 +154,9 @@ def test_noise_rate_with_ddpm_update_needs_slot0_noisier_than_slot1():
     assert st != B.SDS_ERR_INVALID_ARG or "s_min" not in B.sds_last_error()
     if ptr:
         B.lib().sds_destroy(C.c_void_p(ptr))
+
+
+def test_txt2img_with_the_noise_rate_is_rejected():
+    cfg = B.config_from_workload(W.get_config("c1_tiny", cfg_type=0, txt2img=1, noise_rate_on=1))
+    st, _ = _create_status(cfg)
+    assert st == B.SDS_ERR_INVALID_ARG and "noise_rate_on" in B.sds_last_error()

@@ -169,6 +169,31 @@ def test_noise_rate_sets_the_incoming_frames_timestep(update_kind, streams):
     run_sequence(w, 8)
 
 
+@pytest.mark.parametrize("cfg_type,update_kind", [(1, 0), (2, 1)])
+def test_bf16_noise_predictions(cfg_type, update_kind):
+    """eps_c handed over as bf16 (the network's usual output dtype): the
+    update widens it exactly, so it matches the oracle fed the same values."""
+    t_index = [0, 16, 32, 45] if update_kind == 1 else [32, 45]
+    w = W.get_config("c1_tiny", eps_c_bf16=1, cfg_type=cfg_type, update_kind=update_kind,
+                     n=len(t_index), t_index=t_index, steps=4)
+    run_sequence(w, 4)
+
+
+@pytest.mark.parametrize("cfg_type,bf16", [(0, 0), (2, 1)])
+def test_txt2img_incoming_frame_is_the_noise_draw(cfg_type, bf16):
+    """txt2img: no input image, so the incoming latent is eps_new itself
+    (x0_new is passed as NULL); everything else as in img2img."""
+    w = W.get_config("c1_tiny", txt2img=1, cfg_type=cfg_type, eps_c_bf16=bf16, steps=4)
+    g = GpuPipe(w)
+    try:
+        lat = W.gen_latents(w, 0)
+        xn, _ = g.step(lat, None, None, W.LatentWalk(w).next())
+        assert np.array_equal(xn[0], lat["eps_new"])  # bit-exact copy of the draw
+    finally:
+        g.close()
+    run_sequence(w, 4)
+
+
 def test_c3_full_size_with_noise_rate_application():
     w = W.get_config("c3_dit1p3b_video", noise_rate_on=1, burst_prob=0.5)
     run_sequence(w, 4, rows_per_step=8, attend_every=3)

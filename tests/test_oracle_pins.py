@@ -662,3 +662,24 @@ def test_noise_rate_follows_motion_into_the_entry_timestep():
     assert abs(s - (0.3 + 0.5 * (0.9 - 0.3))) < 1e-12    # one EMA step of lambda = 0.5 toward s_max
     st.step_update(z(2, N), z(2, N), z(2, N), z(1, N), z(N), z(N))
     assert st.slot0_timestep() == int(math.floor(s * (w["n_train"] - 1) + 0.5))
+
+
+# --------------------------------------------------------------- txt2img
+
+def test_txt2img_incoming_frame_is_the_noise_draw_and_matches_an_equivalent_img2img_frame():
+    """With no input image the incoming latent is the N(0, I) draw itself.
+    The same latent arises in img2img from the input x0 = eps (1 - sqrt(1 -
+    abar_0)) / sqrt(abar_0), so the two paths agree on everything else."""
+    w = tiny(n=2, cfg_type=0, txt2img=1)
+    N = w["N_s"]
+    rng = np.random.default_rng(11)
+    x, x0, ec = (rng.standard_normal((2, N)).astype(np.float32) for _ in range(3))
+    z = rng.standard_normal((1, N)).astype(np.float32)
+    eps = rng.standard_normal(N).astype(np.float32)
+    xn_t, out_t = O.Stream(w).step_update(x, x0, ec, z, None, eps)
+    assert np.array_equal(xn_t[0], eps.astype(np.float64))
+    ab0 = O.alpha_bar(w)[(w["n_train"] - 1) - w["t_index"][0] * (w["n_train"] // w["n_inf"])]
+    x0_equiv = eps.astype(np.float64) * (1 - math.sqrt(1 - ab0)) / math.sqrt(ab0)
+    xn_i, out_i = O.Stream(dict(w, txt2img=0)).step_update(x, x0, ec, z, x0_equiv.astype(np.float32), eps)
+    assert np.allclose(xn_i[0], eps, rtol=0, atol=1e-6)   # up to the fp32 rounding of x0_equiv
+    assert np.array_equal(xn_i[1], xn_t[1]) and np.array_equal(out_i, out_t)
