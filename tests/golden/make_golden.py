@@ -53,6 +53,33 @@ def compute() -> dict:
     out["ssf"] = ssf
     out["motion"] = mot
     st.close()
+    # guidance / update / entry variants of one step (first 6 elements)
+    variants = {}
+    for name, kw in (("supplied_negative_ddpm", dict(cfg_type=2, update_kind=1, n=4,
+                                                     t_index=[0, 16, 32, 45])),
+                     ("txt2img_no_guidance", dict(cfg_type=0, txt2img=1))):
+        wv = W.get_config("c1_tiny", **kw)
+        sv = O.Stream(wv)
+        lv = W.gen_latents(wv, 1)
+        en = lv["eps_neg"][:, 0] if "eps_neg" in lv else None
+        x0n = None if wv["txt2img"] else lv["x0_new"][0]
+        xn, o = sv.step_update(lv["x"][:, 0], lv["x0"][:, 0], lv["eps_c"][:, 0], lv["z"][:, 0], x0n,
+                               lv["eps_new"][0], eps_neg=en)
+        variants[name] = {"x_next": xn[:, :6].tolist(), "out": o[:6].tolist()}
+        sv.close()
+    out["step_update_variants"] = variants
+    # the noise rate choosing the incoming frame's entry timestep over a walk
+    wr = W.get_config("c1_tiny", noise_rate_on=1, burst_prob=0.5, lat_step=0.3)
+    sr, lwr = O.Stream(wr), W.LatentWalk(wr)
+    entry = []
+    for t in range(6):
+        lr = W.gen_latents(wr, t)
+        sr.step_update(lr["x"][:, 0], lr["x0"][:, 0], lr["eps_c"][:, 0], lr["z"][:, 0],
+                       lr["x0_new"][0], lr["eps_new"][0])
+        m = sr.motion(lwr.next()[0])
+        entry.append([sr.slot0_timestep(), m["s"]])
+    out["noise_rate_entry"] = entry
+    sr.close()
     return out
 
 
