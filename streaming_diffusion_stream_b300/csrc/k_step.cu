@@ -9,7 +9,14 @@
 //       step read as predict-x0-then-re-noise): x0hat, re-noise to the next
 //       slot's level with the supplied z, and noise the incoming frame into
 //       slot 0.  All of an element's inputs are loaded before any of its
-//       outputs is written, so x_next may alias x.
+//       outputs is written, so x_next may alias x.  Variants: a supplied
+//       negative prediction in place of the virtual one (the onetime-negative
+//       R-CFG, or CFG with delta = 1); the strided DDPM posterior step in
+//       place of the re-noise; bf16 noise predictions, widened exactly;
+//       txt2img, where the incoming frame is the noise draw itself; and the
+//       motion noise rate choosing the incoming frame's entry timestep
+//       (StreamDiffusionV2 summary), with slot 0's coefficients then taken
+//       from per-timestep tables.
 //  (ii) StreamDiffusion notes, "Stochastic Similarity Filter": dot and norm
 //       sums of the incoming frame against the reference frame; the frame is
 //       also copied into the spare reference buffer, which becomes current
@@ -23,7 +30,7 @@
 // per quantity.  Reduction work blocks are scheduled before update work
 // blocks; the one that completes the set of partials (an arrival counter)
 // sums them in a fixed order in double (one warp per sum) and takes the
-// decisions (one thread per stream) while the update streams on.  dot, |I|^2 and
+// decisions (one warp per stream) while the update streams on.  dot, |I|^2 and
 // |R|^2 use the same operation sequence, so identical frames give three
 // bitwise-equal sums, cosine exactly 1 and skip probability exactly 1.
 #include "dfloat.cuh"
