@@ -38,6 +38,7 @@ def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_
     g, o = GpuPipe(w), OraclePipe(w)
     emb, lat_walk, frames = W.EmbeddingWalk(w), W.LatentWalk(w), W.FrameWalk(w)
     ssf_live = [True] * S
+    rate_live = [True] * S  # False once a flagged near tie of the entry timestep went the other way
     stats = dict(sink_fires=0, resets=0, skips=0, near=0)
     try:
         for step in range(steps):
@@ -89,14 +90,29 @@ def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_
             frame = frames.next() if ssf else None
             u = W.gen_u(w, step) if ssf else None
             chunk = lat_walk.next() if motion else None
+            # the entry timestep round(s (N-1)) is decided from an s that the
+            # two sides agree on to ~1e-8: flag near half-integers
+            rate_near = [False] * S
+            if w.get("noise_rate_on"):
+                for s in range(S):
+                    xe = o.s[s].noise_rate() * (w["n_train"] - 1) + 0.5
+                    rate_near[s] = abs(xe - round(xe)) < 1e-4
             xn, out = g.step(lat, frame, u, chunk)
             ores = o.step(lat)
+            st = g.state()
+            if w.get("noise_rate_on"):
+                for s in range(S):
+                    if rate_live[s] and st[s]["slot0_timestep"] != o.s[s].slot0_timestep():
+                        assert rate_near[s], (step, s)
+                        rate_live[s] = False  # slot 0 now differs; stop comparing this stream
+                        stats["near"] += 1
             for s in range(S):
+                if not rate_live[s]:
+                    continue
                 xr, outr = ores[s]
                 assert tensor_rel_err(out[s], outr) <= UPD_TOL, (step, s)
                 for i in range(w["n"]):
                     assert tensor_rel_err(xn[i, s], xr[i]) <= UPD_TOL, (step, s, i)
-            st = g.state()
             if ssf:
                 oss = o.ssf(frame, u)
                 for s in range(S):
@@ -111,9 +127,6 @@ def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_
                     assert st[s]["ssf_skip"] == oss[s]["skip"], (step, s, st[s], oss[s])
                     assert st[s]["ssf_skip_count"] == oss[s]["skip_count"]
                     stats["skips"] += oss[s]["skip"]
-            if w.get("noise_rate_on"):
-                for s in range(S):
-                    assert st[s]["slot0_timestep"] == o.s[s].slot0_timestep(), (step, s)
             if motion:
                 om_ = o.motion(chunk)
                 for s in range(S):
