@@ -41,3 +41,22 @@ def test_malformed_lines_are_skipped(tmp_path):
     t0 = 1_800_000_000.0
     s = _sampler(tmp_path, ["garbage", "a, b, c", _row(t0, 2032)])
     assert s.summary(t0 - 0.1, t0 + 0.1)["samples"] == 1
+
+
+def test_workload_flags_and_update_bytes():
+    """The K4 roofline numerator: every operand read once, every result
+    written once (4 B fp32, 2 B for bf16 predictions, no x0_new in txt2img)."""
+    import argparse
+    base = dict(workload="c2_sdturbo_image", streams=None, cfg_type=None, update_kind=None,
+                noise_rate_on=False, eps_c_bf16=False, txt2img=False)
+    w = bench.workload(argparse.Namespace(**base))
+    n, N = w["n"], w["N_s"]
+    # x, x0 (virtual negative), eps_c, x_next per slot; z for n-1; out; x0_new, eps_new
+    assert bench.step_bytes(w, False, False) == 4.0 * N * (4 * n + (n - 1) + 1 + 2)
+    wb = bench.workload(argparse.Namespace(**dict(base, eps_c_bf16=True)))
+    assert bench.step_bytes(wb, False, False) == bench.step_bytes(w, False, False) - 2.0 * N * n
+    wt = bench.workload(argparse.Namespace(**dict(base, txt2img=True)))
+    assert wt["txt2img"] == 1 and wt["cfg_type"] == 0  # no x0, so no self-negative guidance
+    # without guidance there is no negative operand: 4 arrays per slot
+    assert bench.step_bytes(wt, False, False) == 4.0 * N * (3 * n + (n - 1) + 1 + 1)
+    assert bench.step_bytes(w, True, False) - bench.step_bytes(w, False, False) == 12.0 * w["ssf_E"]
