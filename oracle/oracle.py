@@ -59,7 +59,6 @@ def lib():
         L.orc_get_emb.argtypes = [P, P]
         L.orc_key_rows.restype = _i64
         L.orc_key_rows.argtypes = [P, P]
-        L.orc_rotate_queries.argtypes = [P, P, P]
         L.orc_attend.argtypes = [P, P, P, _i64, P]
         L.orc_step_update.argtypes = [P] * 9
         L.orc_step_update2.argtypes = [P] * 10
@@ -221,12 +220,6 @@ class Stream:
         rows = np.zeros(n, dtype=np.int64)
         lib().orc_key_rows(self.h, _p(rows))
         return rows
-
-    def rotate_queries(self, q: np.ndarray) -> np.ndarray:
-        q = np.ascontiguousarray(q, dtype=np.uint16)
-        out = np.zeros_like(q)
-        lib().orc_rotate_queries(self.h, _p(q), _p(out))
-        return out
 
     def attend(self, q: np.ndarray, rows=None) -> np.ndarray:
         """Attention of (unrotated) query rows [n*T*L][H][d]; rotation happens inside."""

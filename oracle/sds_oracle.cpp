@@ -486,31 +486,6 @@ long long orc_key_rows(void* p, long long* rows_out) {
   return n;
 }
 
-// Rotate the query rows of the current chunk (O2) and round them to bf16 --
-// the operand the attention consumes.  q: bf16 [n*T*L][H][d]; qrot same.
-void orc_rotate_queries(void* p, const uint16_t* q, uint16_t* qrot) {
-  Stream* s = (Stream*)p;
-  const orc_cfg& c = s->c;
-  long long TL = c.T * c.L, HD = c.H * c.d;
-  std::vector<double> in((size_t)c.d), out((size_t)c.d);
-  for (long long r = 0; r < c.n * TL; ++r) {
-    long long tok = r % TL;
-    long long j = tok / c.L, l = tok % c.L;
-    long long pos[3] = {s->p0 + j, l / c.grid_w, l % c.grid_w};
-    for (long long h = 0; h < c.H; ++h) {
-      const uint16_t* qr = q + (size_t)(r * HD + h * c.d);
-      uint16_t* orow = qrot + (size_t)(r * HD + h * c.d);
-      if (!c.rope_on) {
-        std::memcpy(orow, qr, (size_t)c.d * 2);
-        continue;
-      }
-      for (long long t = 0; t < c.d; ++t) in[(size_t)t] = bf16_to_double(qr[t]);
-      rope_rotate(in.data(), out.data(), c.d, pos, c.rope_base);
-      for (long long t = 0; t < c.d; ++t) orow[t] = double_to_bf16(out[(size_t)t]);
-    }
-  }
-}
-
 // a4 (video mode): attention of selected query rows against the stream's
 // sink + ring keys.  q: bf16 [n*T*L][H][d] as given (unrotated); each
 // selected row is rotated at its chunk position (O2) and rounded to bf16 --

@@ -251,6 +251,65 @@ def test_pushed_keys_are_rotated_at_their_positions():
                 assert np.array_equal(kb[(w["M"] + slot) * L + l, h], expect)
 
 
+@pytest.mark.parametrize("M", [0, 1])
+def test_query_rows_take_the_positions_of_the_chunk_just_pushed(M):
+    """Which position a query row of orc_attend gets (StreamDiffusionV2
+    summary, "Adaptive sink and RoPE refresh": every slot's queries belong
+    to the chunk just pushed).  Query row r of slot s is token
+    tok = r mod (T*L) of that chunk, frame j = tok // L, grid cell l = tok % L.
+    Feed as queries the chunk's own raw keys, tiled over the n slots: a
+    query is then rotated by the same arithmetic and at the same position as
+    its key, so its rotated bf16 value must equal, bit for bit, the key the
+    push stored for frame j, cell l (whose position is pinned by
+    test_pushed_keys_are_rotated_at_their_positions).  The expected output
+    is the brute-force attention of those stored keys against the key list.
+    A query at another frame, a swapped row/column, or a slot with its own
+    positions changes the rotation and the output by far more than the
+    tolerance.  Runs across a RoPE reset (tau = 3) so p0 takes 0, 2 and 0."""
+    w = tiny(n=3, T=2, R=4, M=M, rope_tau=3)
+    s = O.Stream(w)
+    L, TL, n, gw = w["L"], w["T"] * w["L"], w["n"], w["grid_w"]
+    cells = [0, 3, gw + 5, 2 * gw + 1, 5 * gw + 2, L - 1]  # y != x for most
+    seen_p0 = []
+    F = 0
+    for c in range(3):
+        k, v = _chunk(w, 70 + c)
+        seen_p0.append(s.push(k, v))
+        if M:
+            s.sink_refresh(np.ones(w["D"], dtype=np.float32))
+        first = F
+        F += w["T"]
+        kb, vb = s.kv()
+        keys = s.key_rows()
+        q = np.concatenate([k] * n)  # [n*T*L][H][d]: slot s holds the chunk's keys
+        rows, stored = [], []
+        for sl in range(n):
+            for j in range(w["T"]):
+                for l in cells:
+                    rows.append(sl * TL + j * L + l)
+                    stored.append((M + (first + j) % w["R"]) * L + l)
+        got = s.attend(q, np.array(rows))
+        expect = O.attention(kb[np.array(stored)], kb[keys], vb[keys])
+        np.testing.assert_allclose(got, expect, rtol=0, atol=1e-12)
+        # the slots share the positions: identical outputs for the same token
+        per = len(cells) * w["T"]
+        for sl in range(1, n):
+            assert np.array_equal(got[sl * per:(sl + 1) * per], got[:per])
+    assert seen_p0 == [0, 2, 0]
+    # the check has teeth: a query rotated one frame later (or with its row and
+    # column swapped) gives a clearly different output
+    kb, vb = s.kv()
+    keys = s.key_rows()
+    l = 2 * gw + 1
+    src = _f(k[l])  # frame 0, cell (2, 1) of the last chunk, p0 = 0
+    for pos in ([1, 2, 1], [0, 1, 2]):
+        rot = O.rope_rotate(src, np.array([pos] * w["H"]))
+        wrong = np.array([[O.bf16_round(x) for x in r] for r in rot], dtype=np.uint16)[None]
+        o_wrong = O.attention(wrong, kb[keys], vb[keys])
+        o_right = s.attend(np.concatenate([k] * n), np.array([l]))
+        assert np.max(np.abs(o_wrong - o_right)) > 1e-3
+
+
 def test_sink_fill_then_least_similar_refresh():
     w = tiny(M=2, T=3, R=6, D=2, s_th=0.96, rope=False)
     s = O.Stream(w)
