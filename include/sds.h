@@ -108,12 +108,14 @@ typedef enum {
  * with delta = 1 and unconditional predictions, standard CFG.
  * noise_rate_on: 1 applies the motion-aware noise rate s ([V2] "Motion-aware
  * noise scheduler": the rate adapts the denoising path to the motion) to
- * the incoming frame: it enters slot 0 at timestep t_s = round(s *
- * (num_train_steps - 1)) instead of slot 0's fixed timestep, with the rate
- * decided by the previous step, and the next update treats that frame at
- * t_s (needs motion_on; sds_stream_state.slot0_timestep reports t_s).
- * With update_kind 1, round(s_min * (num_train_steps - 1)) must not fall
- * below slot 1's timestep (else SDS_ERR_INVALID_ARG).
+ * the incoming frame: it enters slot 0 at timestep t_s = t1 + round(s *
+ * (num_train_steps - 1 - t1)), the fraction s of the way from slot 1's
+ * timestep t1 (0 when slots_n == 1) up to pure noise, instead of slot 0's
+ * fixed timestep, so that it is never less noisy than the frame in slot 1
+ * ([SD] "Stream Batch": the slots hold descending timesteps).  The rate is
+ * the one decided by the previous step, and the next update treats that
+ * frame at t_s (needs motion_on and 0 <= s_min <= s_max <= 1;
+ * sds_stream_state.slot0_timestep reports t_s).
  * eps_c_bf16: 1 = the eps_c[i] buffers hold bf16 values (the usual output
  * dtype of the noise-prediction network); the update widens them exactly
  * to fp32.  0 = fp32.
@@ -356,9 +358,12 @@ SDS_API sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds
  * allocator, or in a latency-critical loop where cudaMalloc/cudaFree (which
  * may synchronise the device) are not allowed -- and so cannot create a
  * context.  It computes what sds_ssf computes, on a reference frame the
- * caller supplies instead of the context's stored one, with the same
- * arithmetic (same cosine, probability and decision for the same inputs),
- * and it calls no cudaMalloc, cudaFree or other allocating routine.
+ * caller supplies instead of the context's stored one, with K4's reduction
+ * and decision unchanged (the same work blocks of SDS_NOALLOC_BLOCK_ELEMS
+ * elements, the same per-thread and per-block sums, the same finish): for
+ * the same frame, reference, draw and skip count it returns bit for bit the
+ * cosine, probability and decision that sds_ssf records.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *
  *   frame, ref  device fp32 [S][E]: incoming frame and reference frame
  *   u           device fp32 [S]: uniform draws in [0,1)
@@ -368,16 +373,18 @@ SDS_API sds_status sds_ssf(sds_ctx* ctx, const float* frame, const float* u, sds
  *
  * Scratch: a static device array of SDS_NOALLOC_SCRATCH_BYTES (256 KiB) in
  * the library, present on every GPU that loads the library until the process
- * exits.  Its reduction partials limit the size: S * ceil(E / 2048) * 3 must
- * not exceed SDS_NOALLOC_MAX_PARTIALS (32736; e.g. S <= 28 streams of
+ * exits.  Its reduction partials limit the size: S * ceil(E / 8192) * 3 must
+ * not exceed SDS_NOALLOC_MAX_PARTIALS (32736; e.g. S <= 113 streams of
  * 3x512x512 frames); larger requests fail with SDS_ERR_INVALID_ARG and a
- * message in sds_last_error(NULL).  The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call
- * shares the one array and clears its counter on `stream` before use, so
- * calls whose work overlaps on the GPU (other streams, other host threads)
- * race on it: order them.
+ * message in sds_last_error(NULL).  The first call in a device context looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  A context that
+ * is destroyed and created again (cudaDeviceReset) gets a fresh lookup on
+ * its first call.  Every call shares the one array and clears its counter on
+ * `stream` before use, so calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on it: order them.
  */
+#define SDS_NOALLOC_BLOCK_ELEMS 8192
 #define SDS_NOALLOC_SCRATCH_BYTES 262144
 #define SDS_NOALLOC_MAX_PARTIALS 32736
 SDS_API sds_status sds_ssf_noalloc(const float* frame, const float* ref, const float* u,
@@ -489,6 +496,25 @@ SDS_API sds_status sds_slo_choose(const sds_slo* c, sds_slo_choice* out);
 /* Synchronise `stream` and copy the S per-stream decision records to host
  * memory out[0..S-1]. */
 SDS_API sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stream);
+
+/*
+ * Failure-detection test hook for K1's bounded waits (no counterpart on the
+ * pages).  Every wait of the attention kernel on a barrier gives up after a
+ * time limit (2 s by default); the kernel then records a timeout in the
+ * error word of every stream (sds_stream_state.error_word bit 0), waits,
+ * again bounded, for its own copies in flight, frees its tensor memory and
+ * returns, so the context stays usable.  This call lets a test exercise
+ * that path without a fault: wait_limit_ns (> 0) shortens the limit (0
+ * restores 2 s), and withhold_k_tile >= 0 makes CTA 0 of the following
+ * sds_attend launches skip the copy of that key tile (its counter over the
+ * CTA's tiles), so the waits for it run out; -1 turns that off.  Outputs of
+ * a launch that timed out are undefined.  With the split-key schedule a
+ * timed-out CTA leaves its arrival counters behind, so use it only on
+ * problems of one work item per CTA (attn_ctas 0 and a small problem).
+ * Errors: SDS_ERR_INVALID_ARG.
+ */
+SDS_API sds_status sds_test_attn_timeout(sds_ctx* ctx, int64_t wait_limit_ns,
+                                         int64_t withhold_k_tile);
 
 /* Host-side ring metadata (no device access). */
 SDS_API sds_status sds_get_meta(const sds_ctx* ctx, sds_meta* out);

@@ -549,13 +549,18 @@ void orc_step_update2(void* p, const float* x, const float* x0, const float* eps
   const orc_cfg& c = s->c;
   long long N = c.N_s;
   // reading of the motion-aware noise scheduler: the noise rate s chooses
-  // the timestep at which the incoming frame enters slot 0,
-  // round(s (N_train - 1)); the frame then in slot 0 sits at the timestep it
-  // entered at.  The rate is the one in force before this step's motion.
+  // the timestep at which the incoming frame enters slot 0, as the fraction
+  // s of the way from slot 1's timestep t1 up to pure noise (N_train - 1):
+  // t1 + round(s (N_train - 1 - t1)), with t1 = 0 when there is no slot 1.
+  // So the entering frame is never less noisy than the frame it precedes
+  // and the stream batch's timesteps stay in descending order.  The frame
+  // then in slot 0 sits at the timestep it entered at.  The rate is the one
+  // in force before this step's motion.
   long long t_new = slot_timestep(c, 0);
   if (c.noise_rate_on) {
-    t_new = (long long)std::floor(s->s_rate * (double)(c.n_train - 1) + 0.5);
-    t_new = std::min(std::max(t_new, 0LL), c.n_train - 1);
+    const long long t1 = c.n > 1 ? slot_timestep(c, 1) : 0;
+    t_new = t1 + (long long)std::floor(s->s_rate * (double)(c.n_train - 1 - t1) + 0.5);
+    t_new = std::min(std::max(t_new, t1), c.n_train - 1);
   }
   for (long long i = 0; i < c.n; ++i) {
     long long ti = (i == 0 && c.noise_rate_on) ? s->slot0_t : slot_timestep(c, i);

@@ -105,6 +105,7 @@ SIGNATURES = {
     "sds_ssf": (C.c_int, [_P, _P, _P, _P]),
     "sds_ssf_noalloc": (C.c_int, [_P, _P, _P, _P, _i64, _i64, _f64, _i64, _P, _P, _P, _P]),
     "sds_read_state": (C.c_int, [_P, C.POINTER(sds_stream_state), _P]),
+    "sds_test_attn_timeout": (C.c_int, [_P, _i64, _i64]),
     "sds_get_meta": (C.c_int, [_P, C.POINTER(sds_meta)]),
     "sds_get_buffers": (C.c_int, [_P, C.POINTER(sds_buffers)]),
     "sds_state_export": (C.c_int, [_P, _P, C.POINTER(C.c_size_t), _i64, _P]),
@@ -254,6 +255,10 @@ def make_step_io(x, x0, eps_c, z, x_next, out, x0_new, eps_new, ssf_frame=None, 
 
 def sds_step_update(ctx, io: sds_step_io, stream=None):
     check(lib().sds_step_update(ctx, C.byref(io), _stream(stream)), ctx)
+
+
+def sds_test_attn_timeout(ctx, wait_limit_ns: int, withhold_k_tile: int):
+    check(lib().sds_test_attn_timeout(ctx, int(wait_limit_ns), int(withhold_k_tile)), ctx)
 
 
 def sds_ssf(ctx, frame, u, stream=None):

@@ -35,45 +35,15 @@
 // bitwise-equal sums, cosine exactly 1 and skip probability exactly 1.
 #include "dfloat.cuh"
 #include "sds_internal.h"
+#include "ssf_reduce.cuh"
 
 namespace sds {
 namespace {
 
-__device__ __forceinline__ double warp_sum(double v) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 constexpr int kWarps = kStepThreads / 32;
 
-// Block-wide fixed-order sums of three compensated values per thread
-// (butterfly within each warp, then the warps in index order); the results
-// are valid in thread 0.
-__device__ __forceinline__ void block_sum3(dfloat& a, dfloat& b, dfloat& c, dfloat* red) {
-  a = df_warp_sum(a);
-  b = df_warp_sum(b);
-  c = df_warp_sum(c);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    red[warp] = a;
-    red[kWarps + warp] = b;
-    red[2 * kWarps + warp] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    a = red[0];
-    b = red[kWarps];
-    c = red[2 * kWarps];
-    for (int w = 1; w < kWarps; ++w) {
-      a = df_add(a, red[w]);
-      b = df_add(b, red[kWarps + w]);
-      c = df_add(c, red[2 * kWarps + w]);
-    }
-  }
-  __syncthreads();
-}
-
-// The same for one value.
+// Block-wide fixed-order sum of one compensated value per thread (as
+// block_sum3 of ssf_reduce.cuh); the result is valid in thread 0.
 __device__ __forceinline__ void block_sum1(dfloat& a, dfloat* red) {
   a = df_warp_sum(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -208,11 +178,10 @@ __device__ void update_block(const StepParams& p, int64_t w) {
   st4(p.x_next[0] + e, p.txt2img ? en : noise4(xn, en, new_sa, new_s1a));
 }
 
-// SSF and motion work blocks cover kRedBlockElems elements: 8 float4 per
-// array per thread, all loads in flight before any arithmetic.  Each thread
-// sums in fp32 over 8 consecutive elements of its own (two float4) and in
-// double beyond.
-constexpr int kRedVec = kRedBlockElems / (kStepThreads * 4);  // float4 per thread per array
+// SSF and motion work blocks cover kRedBlockElems elements: kRedVec float4
+// per array per thread, all loads in flight before any arithmetic.  Each
+// thread sums in fp32 over 8 consecutive elements of its own (two float4)
+// and in compensated fp32 pairs beyond (ssf_reduce.cuh).
 
 __device__ void ssf_block(const StepParams& p, int64_t w, dfloat* red) {
   const int64_t s = w / p.nb_s, b = w % p.nb_s;
@@ -235,22 +204,8 @@ __device__ void ssf_block(const StepParams& p, int64_t w, dfloat* red) {
     const int64_t e = base + k * (kStepThreads * 4);
     if (e < p.E) st4(Rn + e, a[k]);
   }
-  dfloat sd = df_make(0.f), si = df_make(0.f), sr = df_make(0.f);
-#pragma unroll
-  for (int k = 0; k < kRedVec; k += 2) {
-    float dot = 0.f, ni = 0.f, nr = 0.f;
-#pragma unroll
-    for (int k2 = k; k2 < k + 2; ++k2) {
-      const float4 x = a[k2], y = r[k2];
-      dot = __fmaf_rn(x.x, y.x, dot); ni = __fmaf_rn(x.x, x.x, ni); nr = __fmaf_rn(y.x, y.x, nr);
-      dot = __fmaf_rn(x.y, y.y, dot); ni = __fmaf_rn(x.y, x.y, ni); nr = __fmaf_rn(y.y, y.y, nr);
-      dot = __fmaf_rn(x.z, y.z, dot); ni = __fmaf_rn(x.z, x.z, ni); nr = __fmaf_rn(y.z, y.z, nr);
-      dot = __fmaf_rn(x.w, y.w, dot); ni = __fmaf_rn(x.w, x.w, ni); nr = __fmaf_rn(y.w, y.w, nr);
-    }
-    sd = df_add(sd, df_make(dot));
-    si = df_add(si, df_make(ni));
-    sr = df_add(sr, df_make(nr));
-  }
+  dfloat sd, si, sr;
+  ssf_accumulate(a, r, sd, si, sr);
   block_sum3(sd, si, sr, red);
   if (threadIdx.x == 0) {
     double* part = p.partials + (s * p.nb_s + b) * 3;
@@ -328,11 +283,7 @@ __device__ void decide(const StepParams& p, int64_t s, const double* vals, int l
       const double dot = vals[0], ni = vals[1], nr = vals[2];
       double cosv = 0.0, P = 0.0;
       int64_t skip = 0;
-      if (has_ref) {
-        cosv = (ni > 0.0 && nr > 0.0) ? dot / sqrt(ni * nr) : 0.0;
-        P = fmin(1.0, fmax(0.0, (cosv - p.eta) / (1.0 - p.eta)));
-        skip = (u < P && count < p.max_skip) ? 1 : 0;
-      }
+      if (has_ref) skip = ssf_decision(dot, ni, nr, p.eta, u, count, p.max_skip, cosv, P);
       st->pub.ssf_skip_count = skip ? count + 1 : 0;
       st->ssf_cur = skip ? cur : (cur ^ 1);
       st->pub.ssf_has_ref = skip ? has_ref : 1;
@@ -383,9 +334,11 @@ __device__ void decide(const StepParams& p, int64_t s, const double* vals, int l
       st->mot_count = count_new;
       st->pub.motion_pairs = pairs + n_new;
       st->pub.noise_rate = new_rate;
-      // the next step's incoming frame enters at round(rate (N - 1))
-      int64_t t_entry = (int64_t)floor(new_rate * (double)(p.n_train - 1) + 0.5);
-      t_entry = t_entry < 0 ? 0 : (t_entry > p.n_train - 1 ? p.n_train - 1 : t_entry);
+      // the next step's incoming frame enters the fraction `rate` of the way
+      // from slot 1's timestep up to N - 1
+      const int64_t t1 = p.t_floor;
+      int64_t t_entry = t1 + (int64_t)floor(new_rate * (double)(p.n_train - 1 - t1) + 0.5);
+      t_entry = t_entry < t1 ? t1 : (t_entry > p.n_train - 1 ? p.n_train - 1 : t_entry);
       st->entry_t_buf[p.par ^ 1] = t_entry;
       st->pub.motion_dhat = dhat;
       st->mot_has_prev = 1;
@@ -420,9 +373,7 @@ __device__ void finalize(const StepParams& p, double* fin) {
         n = p.nb_m;
         stride = 1;
       }
-      double v = 0.0;
-      for (int64_t i = lane; i < n; i += 32) v += __ldcg(base + i * stride);
-      v = warp_sum(v);
+      const double v = partials_sum(base, n, stride, lane);
       if (lane == 0) fin[k] = q < n_ssf ? v : sqrt(v / (double)p.N_f);
     }
     __syncthreads();

@@ -28,10 +28,12 @@ struct sds_ctx {
   float* mot_prev = nullptr;  // [2][S][N_f]
   DevState* state = nullptr;  // [S]
   double* partials = nullptr;
-  unsigned int* counters = nullptr;  // [1 + S]
+  unsigned int* counters = nullptr;  // [1]: K4's arrival counter
   void* attn_ws = nullptr;           // split-key workspace of the attention kernel
   float* coef_dev = nullptr;         // per-timestep coefficients (noise-rate application)
   int64_t step_calls = 0;            // sds_step_update calls (parity of the rate buffers)
+  uint64_t attn_wait_ns = kAttnWaitNs;  // K1's wait limit (shortened only by the test hook)
+  int64_t attn_withhold_k = -1;         // K1 test hook: key tile CTA 0 does not load
   std::vector<void*> allocs;
   // tables
   int rope_seg[3] = {0, 0, 0};
@@ -145,13 +147,9 @@ sds_status validate(const sds_config* c, std::string& why) {
     if (!(c->mot_sigma > 0.0)) return bad("mot_sigma must be > 0");
     if (!(c->s_min <= c->s_max)) return bad("s_min must be <= s_max");
   }
-  if (c->noise_rate_on && c->update_kind == 1 && c->slots_n > 1) {
-    // the strided DDPM step from slot 0 to slot 1 needs slot 0 at least as
-    // noisy as slot 1 whatever timestep the rate picks (alpha <= 1)
-    const int64_t t_lo = (int64_t)std::floor(c->s_min * (double)(c->num_train_steps - 1) + 0.5);
-    const int64_t t1 = (c->num_train_steps - 1) - c->t_index[1] * (c->num_train_steps / c->num_inference_steps);
-    if (t_lo < t1) return bad("noise_rate_on with update_kind 1 needs round(s_min (N-1)) >= slot 1's timestep");
-  }
+  if (c->noise_rate_on && (!(c->s_min >= 0.0) || !(c->s_max <= 1.0)))
+    return bad("noise_rate_on needs 0 <= s_min <= s_max <= 1 (the rate places the incoming frame "
+               "between slot 1's timestep and pure noise)");
   return SDS_OK;
 }
 
@@ -175,6 +173,18 @@ void free_all(sds_ctx* c) {
 
 sds_status cuda_fail(sds_ctx* c, cudaError_t e, const char* what) {
   return fail(c, SDS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// The noise rate places the incoming frame the fraction s of the way from
+// slot 1's timestep t1 (0 with one slot) up to N - 1.
+int64_t entry_floor(const sds_config& c) {
+  return c.slots_n > 1 ? (c.num_train_steps - 1) - c.t_index[1] * (c.num_train_steps / c.num_inference_steps) : 0;
+}
+
+int64_t entry_timestep(const sds_config& c, double s) {
+  const int64_t t1 = entry_floor(c);
+  const int64_t t = t1 + (int64_t)std::floor(s * (double)(c.num_train_steps - 1 - t1) + 0.5);
+  return std::min<int64_t>(std::max<int64_t>(t, t1), c.num_train_steps - 1);
 }
 
 void fill_attn_rope(const sds_ctx* c, AttnParams& ap) {
@@ -332,7 +342,7 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   const size_t coef_bytes = c.noise_rate_on ? (size_t)c.num_train_steps * 7 * 4 : 0;
   const size_t bytes = coef_bytes + (size_t)kv_elems * 2 * 2 + (size_t)emb * 4 + (size_t)tab_entries * 8 +
                        (size_t)ssf_ref * 4 + (size_t)mot_prev * 4 + (size_t)S * sizeof(DevState) +
-                       (size_t)partials * 8 + (size_t)(S + 1) * 4 + ws_bytes;
+                       (size_t)partials * 8 + (size_t)4 + ws_bytes;
   if (c.mem_cap_bytes > 0 && bytes > (size_t)c.mem_cap_bytes)
     return fail(nullptr, SDS_ERR_OOM, "context needs %zu bytes > mem_cap_bytes %lld", bytes,
                 (long long)c.mem_cap_bytes);
@@ -383,7 +393,7 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
   ALLOC(ctx->mot_prev, mot_prev * 4);
   ALLOC(ctx->state, S * (int64_t)sizeof(DevState));
   ALLOC(ctx->partials, partials * 8);
-  ALLOC(ctx->counters, (S + 1) * 4);
+  ALLOC(ctx->counters, 4);
   ALLOC(ctx->attn_ws, ws_bytes);
   ALLOC(ctx->coef_dev, coef_bytes);
 #undef ALLOC
@@ -414,8 +424,7 @@ sds_status sds_create(const sds_config* cfg, sds_ctx** out) {
       std::memset(&d, 0, sizeof d);
       d.pub.sink_j = -1;
       d.pub.noise_rate = c.s_min;
-      int64_t te = (int64_t)std::floor(c.s_min * (double)(c.num_train_steps - 1) + 0.5);
-      te = std::min<int64_t>(std::max<int64_t>(te, 0), c.num_train_steps - 1);
+      const int64_t te = entry_timestep(c, c.s_min);
       d.entry_t_buf[0] = d.entry_t_buf[1] = te;
       const int64_t t0 = (c.num_train_steps - 1) - c.t_index[0] * (c.num_train_steps / c.num_inference_steps);
       d.slot0_t_buf[0] = d.slot0_t_buf[1] = t0;
@@ -546,7 +555,6 @@ sds_status sds_sink_refresh(sds_ctx* ctx, const float* chunk_emb, sds_stream_t s
   p.kv_k = reinterpret_cast<uint4*>(ctx->kv_k);
   p.kv_v = reinterpret_cast<uint4*>(ctx->kv_v);
   p.state = ctx->state;
-  p.counters = ctx->counters + 1;
   p.S = c.streams;
   p.D = c.emb_dim_D;
   p.M = c.sink_M;
@@ -583,6 +591,11 @@ static sds_status attend_common(sds_ctx* ctx, const CUtensorMap& tq, const CUten
     ap.ws_cnt = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ctx->attn_ws) +
                                                 per_rec * ((size_t)head_dim * 4 + 8));
     ap.grid = (int32_t)ctx->cfg.attn_ctas;
+    ap.wait_ns = ctx->attn_wait_ns;
+    ap.withhold_k = ctx->attn_withhold_k;
+  } else {
+    ap.wait_ns = kAttnWaitNs;
+    ap.withhold_k = -1;
   }
   cudaError_t e = launch_attention(tq, tk, tv, ap, head_dim, S, sm_count, st);
   if (e != cudaSuccess) {
@@ -756,6 +769,7 @@ sds_status sds_step_update(sds_ctx* ctx, const sds_step_io* io, sds_stream_t str
   p.par = (int32_t)(ctx->step_calls & 1);
   p.coef_tab = ctx->coef_dev;
   p.n_train = c.num_train_steps;
+  p.t_floor = entry_floor(c);
   if (c.cfg_type != 0) {
     p.c_gamma = (float)c.gamma;
     p.c_dg = (float)(c.delta * (1.0 - c.gamma));
@@ -907,6 +921,17 @@ sds_status sds_read_state(sds_ctx* ctx, sds_stream_state* out, sds_stream_t stre
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "read_state");
   for (int64_t s = 0; s < S; ++s) out[s] = tmp[(size_t)s].pub;
+  return SDS_OK;
+}
+
+sds_status sds_test_attn_timeout(sds_ctx* ctx, int64_t wait_limit_ns, int64_t withhold_k_tile) {
+  if (!ctx) return fail(nullptr, SDS_ERR_INVALID_ARG, "ctx is NULL");
+  if (wait_limit_ns < 0 || wait_limit_ns > (int64_t)kAttnWaitNs || withhold_k_tile < -1)
+    return fail(ctx, SDS_ERR_INVALID_ARG,
+                "test_attn_timeout: wait_limit_ns must be in [0, 2e9] (0: default) and "
+                "withhold_k_tile >= -1");
+  ctx->attn_wait_ns = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kAttnWaitNs;
+  ctx->attn_withhold_k = withhold_k_tile;
   return SDS_OK;
 }
 

@@ -64,7 +64,11 @@ struct AttnParams {
   float2* ws_ml;         // [kAttnMaxCtas][2][2][128] partial (running max, sum)
   unsigned int* ws_cnt;  // [kAttnMaxCtas][2][128] arrival counters, zero between launches
   int32_t grid;          // CTAs of the persistent schedule (0: the device's SM count)
+  uint64_t wait_ns;      // limit of every wait on a barrier (kAttnWaitNs unless a test shortens it)
+  int64_t withhold_k;    // test hook: >= 0 makes CTA 0 skip the key copy of that tile (-1: off)
 };
+
+constexpr uint64_t kAttnWaitNs = 2000000000ull;  // 2 s
 
 constexpr int kAttnMaxCtas = 160;  // >= the SM count of the target part (148)
 // Bytes of the split-key workspace for head_dim d.
@@ -100,14 +104,14 @@ struct SinkParams {
   float* emb;           // [S][M][D]
   uint4* kv_k;          // bf16 [S][(M+R)*L][H*d]
   uint4* kv_v;
-  DevState* state;
-  unsigned int* counters;  // [S], zero between launches
+  DevState* state;       // the decision kernel's record, read by the copy kernel
   int64_t S, D, M, R, L, HD;
   int64_t chunk_first;  // global index of frame 0 of the chunk just pushed
   int64_t fill_from;    // >= 0: fill mode, first empty sink; < 0: similarity test
   int64_t fill_count;
   double s_th;
 };
+// Two launches: the decision (one block per stream), then the copy.
 cudaError_t launch_sink_refresh(const SinkParams& p, int sm_count, cudaStream_t st);
 
 // ----------------------------------------------------------------- K4
@@ -142,6 +146,7 @@ struct StepParams {
   // timestep: 1/sqrt(alpha), (1-alpha)/(sqrt(alpha) sqrt(1-abar)), sigma
   const float* coef_tab;
   int64_t n_train;
+  int64_t t_floor;                 // slot 1's timestep (0 with one slot): the lowest entry timestep
   int32_t n;                       // slots (0: no update segment)
   int64_t N_s;
   // SSF segment

@@ -140,18 +140,19 @@ def test_raw_attention_rejects_bad_sizes_without_cuda():
     assert L.sds_attention(p + 2, p, p, p, 1, 8, 8, 1, 64, None) == B.SDS_ERR_INVALID_ARG
 
 
-def test_noise_rate_with_ddpm_update_needs_slot0_noisier_than_slot1():
-    """With the strided DDPM update the rate's lowest entry timestep,
-    round(s_min (N-1)), may not fall below slot 1's timestep (alpha > 1)."""
-    w = W.get_config("c1_tiny", noise_rate_on=1, update_kind=1)
-    cfg = B.config_from_workload(w)
-    t1 = (w["n_train"] - 1) - w["t_index"][1] * (w["n_train"] // w["n_inf"])
-    cfg.s_min = (t1 - 1) / (w["n_train"] - 1)
-    st, _ = _create_status(cfg)
-    assert st == B.SDS_ERR_INVALID_ARG and "s_min" in B.sds_last_error()
-    cfg.s_min = t1 / (w["n_train"] - 1)
-    st, ptr = _create_status(cfg)
-    assert st != B.SDS_ERR_INVALID_ARG or "s_min" not in B.sds_last_error()
+def test_noise_rate_needs_a_rate_inside_the_unit_interval():
+    """The rate places the incoming frame the fraction s of the way from slot
+    1's timestep to pure noise, so with the rate applied s_min and s_max must
+    lie in [0, 1]; any such config is accepted by validation, with either
+    update, since the entry is never below slot 1."""
+    w = W.get_config("c1_tiny", noise_rate_on=1, update_kind=1, s_min=0.0, s_max=1.0)
+    for field, value in (("s_min", -0.1), ("s_max", 1.5)):
+        cfg = B.config_from_workload(w)
+        setattr(cfg, field, value)
+        st, _ = _create_status(cfg)
+        assert st == B.SDS_ERR_INVALID_ARG and "s_min <= s_max <= 1" in B.sds_last_error()
+    st, ptr = _create_status(B.config_from_workload(w))
+    assert st != B.SDS_ERR_INVALID_ARG  # no GPU here: creation stops later, at the device
     if ptr:
         B.lib().sds_destroy(C.c_void_p(ptr))
 

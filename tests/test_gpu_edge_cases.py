@@ -16,6 +16,7 @@ and the EMA s + (1 - lambda)(s_min - s) leaves s_min unchanged.
 import numpy as np
 import pytest
 
+from oracle import oracle as O
 from streaming_diffusion_stream_b300 import workloads as W
 from tests.harness import GpuPipe, OraclePipe, tensor_rel_err
 
@@ -87,12 +88,13 @@ def test_zero_skip_cap_processes_every_frame():
 def test_identical_motion_frames_hold_the_noise_rate_at_s_min(T, rate_on):
     """Chunks whose frames never change: every pair's motion is exactly 0,
     dhat is 0, and the noise rate stays exactly s_min (with the rate applied,
-    the incoming frame enters at round(s_min (N - 1)) every step)."""
+    the incoming frame enters at the timestep of rate s_min every step)."""
     w = W.get_config("c1_tiny", T=T, R=max(4, T), mot_k=T, noise_rate_on=rate_on, streams=2)
     g, o = GpuPipe(w), OraclePipe(w)
     still = W.LatentWalk(w).next()[:, :1, :]              # [S][1][N_f]
     chunk = np.ascontiguousarray(np.repeat(still, T, axis=1))
-    t_entry = int(np.floor(w["s_min"] * (w["n_train"] - 1) + 0.5))
+    t1 = O.slot_timestep(w, 1)  # the entry runs from slot 1's timestep (rate 0) to N - 1 (rate 1)
+    t_entry = t1 + int(np.floor(w["s_min"] * (w["n_train"] - 1 - t1) + 0.5))
     try:
         for step in range(5):
             lat = W.gen_latents(w, step)

@@ -12,6 +12,7 @@ of the tensor max; cosines within 1e-6; motion and noise rate within 1e-5.
 import numpy as np
 import pytest
 
+from oracle import oracle as O
 from streaming_diffusion_stream_b300 import workloads as W
 from tests.harness import (GpuPipe, OraclePipe, attn_rel_err, rope_k_excess, tensor_rel_err)
 
@@ -90,12 +91,13 @@ def run_sequence(w: dict, steps: int, rows_per_step=None, attend_every=1, check_
             frame = frames.next() if ssf else None
             u = W.gen_u(w, step) if ssf else None
             chunk = lat_walk.next() if motion else None
-            # the entry timestep round(s (N-1)) is decided from an s that the
-            # two sides agree on to ~1e-8: flag near half-integers
+            # the entry timestep t1 + round(s (N - 1 - t1)) is decided from an
+            # s that the two sides agree on to ~1e-8: flag near half-integers
             rate_near = [False] * S
             if w.get("noise_rate_on"):
+                t1 = O.slot_timestep(w, 1) if w["n"] > 1 else 0
                 for s in range(S):
-                    xe = o.s[s].noise_rate() * (w["n_train"] - 1) + 0.5
+                    xe = o.s[s].noise_rate() * (w["n_train"] - 1 - t1) + 0.5
                     rate_near[s] = abs(xe - round(xe)) < 1e-4
             xn, out = g.step(lat, frame, u, chunk)
             ores = o.step(lat)

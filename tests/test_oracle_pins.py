@@ -685,9 +685,10 @@ def test_ddpm_adjacent_step_noise_scale_is_beta_tilde():
 # --------------------------------------------------------------- noise-rate application
 
 def test_noise_rate_sets_the_entry_timestep_and_the_next_update_uses_it():
-    """With the rate at s_min (no motion yet) the incoming frame enters at
-    round(s_min (N - 1)); next step the frame in slot 0 is treated at that
-    timestep: built from its x0 and true noise at that level, it predicts x0."""
+    """With the rate at s_min (no motion yet) and one slot (nothing below
+    slot 0), the incoming frame enters at round(s_min (N - 1)); next step the
+    frame in slot 0 is treated at that timestep: built from its x0 and true
+    noise at that level, it predicts x0."""
     w = tiny(n=1, T=1, noise_rate_on=1, cfg_type=0, s_min=0.3, s_max=0.9)
     st = O.Stream(w)
     N = w["N_s"]
@@ -710,7 +711,8 @@ def test_noise_rate_sets_the_entry_timestep_and_the_next_update_uses_it():
 
 def test_noise_rate_follows_motion_into_the_entry_timestep():
     """A burst that clips the motion to 1 drives the rate toward s_max, and
-    the next incoming frame enters at round(rate (N - 1))."""
+    the next incoming frame enters the fraction `rate` of the way from slot
+    1's timestep (99 for t_index [32, 45]) to N - 1."""
     w = tiny(n=2, T=1, noise_rate_on=1, mot_k=1, sigma=1.0, lam=0.5)
     st = O.Stream(w)
     N, Nf = w["N_s"], w["N_f"]
@@ -720,7 +722,40 @@ def test_noise_rate_follows_motion_into_the_entry_timestep():
     s = st.noise_rate()
     assert abs(s - (0.3 + 0.5 * (0.9 - 0.3))) < 1e-12    # one EMA step of lambda = 0.5 toward s_max
     st.step_update(z(2, N), z(2, N), z(2, N), z(1, N), z(N), z(N))
-    assert st.slot0_timestep() == int(math.floor(s * (w["n_train"] - 1) + 0.5))
+    t1 = O.slot_timestep(w, 1)
+    assert t1 == 99
+    assert st.slot0_timestep() == t1 + int(math.floor(s * (w["n_train"] - 1 - t1) + 0.5))
+
+
+def test_entry_timestep_keeps_the_stream_batch_in_descending_order():
+    """StreamDiffusion notes, "Stream Batch": the n slots hold frames at
+    descending timesteps, each frame one denoise step further than the one
+    before it.  Whatever rate the motion sets, the incoming frame must not be
+    less noisy than the frame in slot 1: for the four-slot schedule
+    999 / 679 / 359 / 99 the entry timestep runs from 679 (rate 0) to 999
+    (rate 1), never decreasing as the rate grows.  (lambda = 0 makes the
+    rate equal its target, s_min = 0 and s_max = 1 make the target the
+    clipped motion itself, and a constant shift c has motion |c|.)"""
+    w = tiny(n=4, t_index=[0, 16, 32, 45], T=1, noise_rate_on=1, mot_k=1, sigma=1.0, lam=0.0,
+             s_min=0.0, s_max=1.0, cfg_type=0)
+    assert [O.slot_timestep(w, i) for i in range(4)] == [999, 679, 359, 99]
+    N, Nf = w["N_s"], w["N_f"]
+    zeros = lambda *sh: np.zeros(sh, np.float32)
+    last = -1
+    for c in (0.0, 0.05, 0.25, 0.5, 0.75, 0.95, 1.0, 3.0):
+        st = O.Stream(w)
+        st.motion(zeros(1, Nf))
+        st.motion(np.full((1, Nf), c, np.float32))  # d = |c|
+        assert abs(st.noise_rate() - min(float(np.float32(c)), 1.0)) < 1e-12
+        st.step_update(zeros(4, N), zeros(4, N), zeros(4, N), zeros(3, N), zeros(N), zeros(N))
+        t = st.slot0_timestep()
+        assert 679 <= t <= 999 and t >= last, (c, t)
+        last = t
+        if c == 0.0:
+            assert t == 679
+        if c >= 1.0:
+            assert t == 999
+        st.close()
 
 
 # --------------------------------------------------------------- txt2img
