@@ -71,7 +71,6 @@ namespace {
 constexpr int BM = 128;         // query rows per tile (two tiles per item)
 constexpr int BN = 128;         // keys per tile
 constexpr int SUB = 128 * 128;  // bytes of one 128-row x 64-column bf16 sub-tile
-constexpr int kThreads = 352;   // 8 softmax warps + producer + 2 MMA issuers
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
@@ -92,11 +91,32 @@ struct Cfg {
   static constexpr int ISS = EARLY ? 2 : 1;  // MMA-issuing threads
   static constexpr uint32_t O_COL = EARLY ? 384u : 256u;  // first column of O0
   static constexpr uint32_t O_STRIDE = EARLY ? 64u : 128u;
+  // Threads per query row (HV, "halves"): with two, each of the two threads
+  // of a row takes half of its score columns, P columns and O columns, so
+  // that a tile has 8 softmax warps (2 per SM sub-partition and tile) and the
+  // exponentials of one warp overlap the score loads and row maxima of
+  // others.  The halves combine their row maxima every tile and their row
+  // sums at the end of an item through shared memory.
+#ifndef SDS_K1_HV64
+#define SDS_K1_HV64 1
+#endif
+#ifndef SDS_K1_TURNS
+#define SDS_K1_TURNS 1
+#endif
+#ifndef SDS_K1_PWAIT_FIRST
+#define SDS_K1_PWAIT_FIRST 1
+#endif
+  static constexpr int HV = (D == 64) ? SDS_K1_HV64 : 1;
+  static constexpr int SMW = 8 * HV;              // softmax warps (two tiles)
+  static constexpr int WP = SMW;                  // TMA producer warp
+  static constexpr int WI = SMW + 1;              // MMA issuer warp(s): WI, WI + 1
+  static constexpr int THREADS = (SMW + 3) * 32;  // softmax + producer + 2 issuer warps
   static constexpr int Q = 0;
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
   static constexpr int BAR = V + ST * TILE;
-  static constexpr int TOTAL = BAR + 512;
+  static constexpr int XCH = BAR + 512;           // row-max [2 parity][2 tile][2 half][128], row-sum [2][2][128]
+  static constexpr int TOTAL = XCH + (HV == 2 ? (8 + 4) * 128 * 4 : 0);
   static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment
 };
 
@@ -124,9 +144,14 @@ struct Bars {
   uint64_t* o_done;  // [2]
   uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
-  uint64_t* tok;        // [2]: group t has finished its exponentials of a tile (EARLY)
+  uint64_t* tok;        // [2]: group t has finished its exponentials of a tile (EARLY, HV 1)
+  uint64_t* xb;         // [2 tile][2 parity]: both halves' row maxima are in shared memory (HV 2)
+  uint64_t* lb;         // [2 tile]: both halves' row sums are in shared memory (HV 2)
+  uint64_t* wb;         // [2 tile]: both halves' partial O rows are written (HV 2, split items)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  float* xmax;          // [2 parity][2 tile][2 half][128]
+  float* xsum;          // [2 tile][2 half][128]
 };
 
 template <int D>
@@ -147,8 +172,13 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.mma_final = r.o_done + 2;
   r.s_free = r.mma_final + 2;
   r.tok = r.s_free + 2;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(r.tok + 2);
+  r.xb = r.tok + 2;
+  r.lb = r.xb + 4;
+  r.wb = r.lb + 2;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.wb + 2);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
+  r.xmax = reinterpret_cast<float*>(sm + C::XCH);
+  r.xsum = r.xmax + 8 * 128;
   return r;
 }
 
@@ -168,11 +198,13 @@ __device__ __forceinline__ void fail_wait(const Bars& B) { *B.abort_flag = 1; }
 // a short inline spin, then the bounded wait out of line, so that the
 // timer bookkeeping (and the register saves of the call) stay off the
 // usual path.
-__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity); }
-__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return mbar_wait(bar, parity, limit_ns);
+}
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   for (int i = 0; i < 1024; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity);
+  return wait_slow(bar, parity, limit_ns);
 }
 
 // The even division of U units over G CTAs: CTA c owns [lo(c), lo(c+1)).
@@ -229,7 +261,7 @@ __device__ __forceinline__ ItemPos item_pos(const AttnParams& p, int64_t item, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using C = Cfg<D>;
@@ -260,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.q_full + i, 1);
       mbar_init(B.q_empty + i, C::EARLY ? 2 : 1);
-      mbar_init(B.q_ready + 2 * i + 0, 128);
-      mbar_init(B.q_ready + 2 * i + 1, 128);
+      mbar_init(B.q_ready + 2 * i + 0, 128 * C::HV);
+      mbar_init(B.q_ready + 2 * i + 1, 128 * C::HV);
     }
     for (int i = 0; i < C::ST; ++i) {
       mbar_init(B.k_full + i, 1);
@@ -271,16 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.s_full + i, 1);
-      mbar_init(B.p_full + i, 128);
+      mbar_init(B.p_full + i, 128 * C::HV);
       mbar_init(B.o_done + i, 1);
       mbar_init(B.mma_final + i, 1);
-      mbar_init(B.s_free + i, 128);
-      mbar_init(B.tok + i, 128);
+      mbar_init(B.s_free + i, 128 * C::HV);
+      mbar_init(B.tok + i, 128 * C::HV);
+      mbar_init(B.xb + 2 * i + 0, 128 * C::HV);
+      mbar_init(B.xb + 2 * i + 1, 128 * C::HV);
+      mbar_init(B.lb + i, 128 * C::HV);
+      mbar_init(B.wb + i, 128 * C::HV);
     }
     *B.abort_flag = 0;
     fence_barrier_init();
   }
-  if (wid == 9) {
+  if (wid == C::WI) {
     tmem_alloc(B.tmem_slot, 512);
     tmem_relinquish();
   }
@@ -289,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *B.tmem_slot;
 
-  if (wid == 8) {
+  if (wid == C::WP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && active) {
       SegIter it;
@@ -304,12 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ItemPos ip = item_pos(p, it.item, npairs);
         int key0, nvalid;
         key_tile(p, nt0, it.kt(), key0, nvalid);
-        if (!mbar_wait(B.k_empty + st, ph ^ 1u)) { ok = false; break; }
-        mbar_arrive_expect_tx(B.k_full + st, C::TILE);
-        for (int b = 0; b < C::NSUB; ++b)
-          tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, ip.h * D + b * 64, key0, ip.s, B.k_full + st);
+        if (!mbar_wait(B.k_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
+        // failure-detection test hook: CTA 0 never loads the keys of tile
+        // `withhold_k`, so every wait for them runs out
+        const bool withhold = p.withhold_k >= 0 && g == p.withhold_k && cta == 0;
+        if (!withhold) {
+          mbar_arrive_expect_tx(B.k_full + st, C::TILE);
+          for (int b = 0; b < C::NSUB; ++b)
+            tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, ip.h * D + b * 64, key0, ip.s, B.k_full + st);
+        }
         issued_k = g + 1;
-        if (!mbar_wait(B.v_empty + st, ph ^ 1u)) { ok = false; break; }
+        if (!mbar_wait(B.v_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
         mbar_arrive_expect_tx(B.v_full + st, C::TILE);
         for (int b = 0; b < C::NSUB; ++b)
           tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
@@ -318,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // this item's queries; the buffer is free once the last S MMAs
           // of the item that used it before have completed
           const int qb = it.sg % C::QB;
-          if (it.sg >= C::QB && !mbar_wait(B.q_empty + qb, (uint32_t)(it.sg / C::QB - 1) & 1u)) {
+          if (it.sg >= C::QB && !mbar_wait(B.q_empty + qb, (uint32_t)(it.sg / C::QB - 1) & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -334,20 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail_wait(B);
       // leave only after every copy we issued has landed in shared memory
       for (int sgi = (issued_q > C::QB ? issued_q - C::QB : 0); sgi < issued_q; ++sgi)
-        mbar_wait(B.q_full + sgi % C::QB, (uint32_t)(sgi / C::QB) & 1u);
+        mbar_wait(B.q_full + sgi % C::QB, (uint32_t)(sgi / C::QB) & 1u, p.wait_ns);
       for (int64_t j = (issued_k > C::ST ? issued_k - C::ST : 0); j < issued_k; ++j)
-        mbar_wait(B.k_full + j % C::ST, (uint32_t)(j / C::ST) & 1u);
+        if (!(p.withhold_k == j && cta == 0)) mbar_wait(B.k_full + j % C::ST, (uint32_t)(j / C::ST) & 1u, p.wait_ns);
       for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
-        mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u);
+        mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u, p.wait_ns);
     }
-  } else if (C::EARLY && (wid == 9 || wid == 10)) {
+  } else if (C::EARLY && (wid == C::WI || wid == C::WI + 1)) {
     // ------------------------------------------------------------ MMA issuers (d = 64):
     // one thread per query tile t, for S_t = Q_t K^T and O_t += P_t V.
     // S_t(g+1) goes out as soon as the softmax has read S_t(g) (s_free) and
     // before P_t(g) exists, so the next scores are ready when the softmax
     // finishes the current tile.
     if (lane == 0 && active) {
-      const int t = wid - 9;
+      const int t = wid - C::WI;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
       const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
@@ -380,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int64_t item = u / nkt;
         const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
-        ok = mbar_wait(B.q_ready + t, 0) && mbar_wait(B.k_full, 0);
+        ok = mbar_wait(B.q_ready + t, 0, p.wait_ns) && mbar_wait(B.k_full, 0, p.wait_ns);
         if (ok) {
           tc_fence_after();
           issue_s(0, 0);
@@ -408,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // at a boundary S_t(g+1) goes after PV_t(g)
           auto next_s = [&]() -> bool {
             const int qb1 = boundary ? qb_n : sg % C::QB;
-            if (!mbar_wait(B.k_full + st1, ph1) || !mbar_wait(B.s_free + t, g & 1u) ||
-                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n)))
+            if (!mbar_wait(B.k_full + st1, ph1, p.wait_ns) || !mbar_wait(B.s_free + t, g & 1u, p.wait_ns) ||
+                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n, p.wait_ns)))
               return false;
             tc_fence_after();
             issue_s(qb1, st1);
@@ -422,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!mbar_wait(B.v_full + st, ph) || !mbar_wait(B.p_full + t, g & 1u)) {
+          if (!mbar_wait(B.v_full + st, ph, p.wait_ns) || !mbar_wait(B.p_full + t, g & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -440,9 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) fail_wait(B);
       mma_commit(B.mma_final + t);
-      mbar_wait(B.mma_final + t, 0);
+      mbar_wait(B.mma_final + t, 0, p.wait_ns);
     }
-  } else if (wid == 9) {
+  } else if (wid == C::WI) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && active) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
@@ -482,12 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int64_t item = u / nkt;
         const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
-        ok = mbar_wait(B.q_ready + 0, 0) && mbar_wait(B.k_full, 0);
+        ok = mbar_wait(B.q_ready + 0, 0, p.wait_ns) && mbar_wait(B.k_full, 0, p.wait_ns);
         if (ok) {
           tc_fence_after();
           issue_s(0, 0, 0);
           mma_commit(B.s_full + 0);
-          ok = mbar_wait(B.q_ready + 1, 0);
+          ok = mbar_wait(B.q_ready + 1, 0, p.wait_ns);
         }
         if (ok) {
           tc_fence_after();
@@ -514,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tile g+1 is the last of its segment: its S MMAs release the Q buffer
           const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
           // the producer lands K/V tiles well ahead: wait for them first
-          if (!mbar_wait(B.v_full + st, ph) || (more && !mbar_wait(B.k_full + st1, ph1))) {
+          if (!mbar_wait(B.v_full + st, ph, p.wait_ns) || (more && !mbar_wait(B.k_full + st1, ph1, p.wait_ns))) {
             ok = false;
             break;
           }
-          if (!mbar_wait(B.p_full + 0, g & 1u)) {
+          if (!mbar_wait(B.p_full + 0, g & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -527,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 0);
           const int qb1 = boundary ? qb_n : sg % C::QB;
           if (more) {
-            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n)) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 0, qp_n, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -535,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(0, qb1, st1);
             mma_commit(B.s_full + 0);
           }
-          if (!mbar_wait(B.p_full + 1, g & 1u)) {
+          if (!mbar_wait(B.p_full + 1, g & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -544,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(B.o_done + 1);
           mma_commit(B.v_empty + st);
           if (more) {
-            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n)) {
+            if (boundary && !mbar_wait(B.q_ready + 2 * qb1 + 1, qp_n, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -561,17 +602,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail_wait(B);
       // all our MMAs complete before tensor memory is released
       mma_commit(B.mma_final + 0);
-      mbar_wait(B.mma_final + 0, 0);
+      mbar_wait(B.mma_final + 0, 0, p.wait_ns);
     }
-  } else if (wid < 8 && active) {
+  } else if (wid < C::SMW && active) {
     // ------------------------------------------------------------ softmax groups
-    const int t = wid >> 2;   // query tile of this group
-    const int r = tid & 127;  // row within the tile == TMEM lane
+    // Warp w: query tile t, half hf of each row's columns, TMEM lanes
+    // 32 (w mod 4) .. +31 (a warp reaches only its own quarter of the lanes).
+    constexpr int HV = C::HV;
+    constexpr int NC = BN / HV;   // score columns of this thread's row
+    constexpr int DC = D / HV;    // O columns of this thread's row
+    const int t = wid / (4 * HV);
+    const int hf = (wid / 4) % HV;
+    const int r = (wid & 3) * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((wid & 3) * 32) << 16;
-    const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_base;
-    const uint32_t tO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE + lane_base;
+    const uint32_t tS = tmem + (uint32_t)(t * 128 + hf * NC) + lane_base;
+    const uint32_t tO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE + (uint32_t)(hf * DC) + lane_base;
     // packed bf16 probabilities: own columns (EARLY) or over the scores
-    const uint32_t tP = C::EARLY ? tmem + 256u + (uint32_t)(t * 64) + lane_base : tS;
+    const uint32_t tP = (C::EARLY ? tmem + 256u + (uint32_t)(t * 64) : tmem + (uint32_t)(t * 128)) +
+                        (uint32_t)(hf * NC / 2) + lane_base;
     // 32 columns of this row's O
     auto load_o = [&](int c, float(&tmp)[32]) {
       tmem_ld32(tO + (uint32_t)(c * 32), tmp);
@@ -582,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 sc2 = make_float2(sc, sc);
     int64_t u = u_lo;
     int sg = 0, g = 0;  // segment and global tile counters (as the other roles count them)
+    int nsplit = 0;     // split segments finished (phase counter of wb)
     bool ok = true;
     while (ok && u < u_hi) {
       // ---- start of an item: its queries
@@ -591,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const ItemPos ip = item_pos(p, item, npairs);
       const int64_t row = ip.q0 + t * BM + r;
       const int qb = sg % C::QB;
-      if (!mbar_wait(B.q_full + qb, (uint32_t)(sg / C::QB) & 1u)) {
+      if (!mbar_wait(B.q_full + qb, (uint32_t)(sg / C::QB) & 1u, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -602,13 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int seg[3] = {p.rope_seg[0], p.rope_seg[1], p.rope_seg[2]};
         const int off[3] = {p.tab_off[0], p.tab_off[1], p.tab_off[2]};
         uint8_t* qt = sQ + (qb * 2 + t) * C::TILE;
-#pragma unroll 1
-        for (int b = 0; b < C::NSUB; ++b) {
+        // this half's share of the row's 16-byte chunks (8 per 64 columns)
+        constexpr int CH = C::NSUB * 8 / HV;
 #pragma unroll 2
-          for (int c = 0; c < 8; ++c) {
-            uint4* ptr = reinterpret_cast<uint4*>(qt + b * SUB + swz(r, c));
-            *ptr = rope8(*ptr, b * 64 + c * 8, pos, seg, p.rope_tab, off);
-          }
+        for (int k = hf * CH; k < (hf + 1) * CH; ++k) {
+          const int b = k >> 3, c = k & 7;
+          uint4* ptr = reinterpret_cast<uint4*>(qt + b * SUB + swz(r, c));
+          *ptr = rope8(*ptr, b * 64 + c * 8, pos, seg, p.rope_tab, off);
         }
         fence_proxy_async_smem();
       }
@@ -616,17 +665,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = -INFINITY, l_run = 0.f;
       // ---- the item's key tiles
       for (int kt = k0; kt < k1; ++kt, ++g) {
-        if (!mbar_wait(B.s_full + t, (uint32_t)g & 1u)) {
+        if (!mbar_wait(B.s_full + t, (uint32_t)g & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float sv[BN / 32][32];
+        float sv[NC / 32][32];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
+        for (int c = 0; c < NC / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) reg_fence32(sv[c]);
+        for (int c = 0; c < NC / 32; ++c) reg_fence32(sv[c]);
         if (C::EARLY) {
           // the scores are in registers: the issuer may overwrite them
           tc_fence_before();
@@ -636,27 +685,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         key_tile(p, nt0, kt, key0, nvalid);
         if (nvalid < BN) {
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            sv[c >> 5][c & 31] = (c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
+          for (int c = 0; c < NC; ++c)
+            sv[c >> 5][c & 31] = (hf * NC + c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
         }
         // P = exp2(s*sc - m) as packed bf16, stored as it is made over the
-        // first 64 columns of S (or, EARLY, P_t's own columns); returns the
-        // row sum of this tile's probabilities.
+        // first half of this thread's S columns (or, EARLY, P_t's own
+        // columns); returns the sum of this thread's probabilities.
         // EARLY: P_t(g) may overwrite P_t(g-1) only once PV_t(g-1) has read it
         auto p_free = [&]() -> bool {
           if (!C::EARLY || g == 0) return true;
-          if (!wait_spin(B.o_done + t, (uint32_t)(g - 1) & 1u)) return false;
+          if (!wait_spin(B.o_done + t, (uint32_t)(g - 1) & 1u, p.wait_ns)) return false;
           tc_fence_after();
           return true;
         };
-        uint32_t pk[4][16];
+        constexpr int NPART = NC / 32;         // 16 packed columns per part
+        // EARLY: P_t(g) may overwrite P_t(g-1) once PV_t(g-1) has read it.
+        // PWAIT_FIRST waits for that before the exponentials (while the
+        // other group may hold the MUFU turn), so the exponentials never
+        // stall and P is stored as it is made; otherwise the first half of
+        // P waits in registers and the wait falls in the middle.
+        constexpr bool PWAIT_FIRST = C::EARLY && SDS_K1_PWAIT_FIRST;
+        constexpr int HOLD = (C::EARLY && !PWAIT_FIRST) ? NPART / 2 : 0;  // parts held until P is free
+        uint32_t pk[NPART][16];
         bool pwait_ok = true;
         auto exp_pass = [&](float m) -> float {
           const float2 nm2 = make_float2(-m, -m);
           float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int part = 0; part < 4; ++part) {
+          for (int part = 0; part < NPART; ++part) {
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const float a0 = sv[part][2 * q], a1 = sv[part][2 * q + 1];
@@ -665,55 +722,72 @@ __global__ void __launch_bounds__(kThreads, 1)
               rs[q & 3] = __fadd2_rn(rs[q & 3], make_float2(e0, e1));
               pk[part][q] = pack_bf16x2(e0, e1);
             }
-            if (!C::EARLY || part >= 2) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
-            if (C::EARLY && part == 1) {
+            if (part >= HOLD) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
+            if (HOLD > 0 && part == HOLD - 1) {
               pwait_ok = p_free();
-              tmem_st16u(tP, pk[0]);
-              tmem_st16u(tP + 16u, pk[1]);
+#pragma unroll
+              for (int h = 0; h < HOLD; ++h) tmem_st16u(tP + (uint32_t)(h * 16), pk[h]);
             }
           }
           const float2 s01 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
           return s01.x + s01.y;
         };
         float alpha = 1.f, m_new, lsum;
-        // EARLY: the two groups take turns at the exponentials (E0(g), E1(g),
-        // E0(g+1), ...), so each runs alone on the MUFU pipe while the other
-        // loads scores and takes its row max
+        // EARLY with one thread per row: the two groups take turns at the
+        // exponentials (E0(g), E1(g), E0(g+1), ...), so each runs alone on
+        // the MUFU pipe while the other loads scores and takes its row max
+        constexpr bool TURNS = C::EARLY && SDS_K1_TURNS;
         auto take_turn = [&]() -> bool {
-          if (!C::EARLY) return true;
-          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u);
-          return wait_spin(B.tok + 0, (uint32_t)g & 1u);
+          if (!TURNS) return true;
+          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u, p.wait_ns);
+          return wait_spin(B.tok + 0, (uint32_t)g & 1u, p.wait_ns);
         };
         auto give_turn = [&]() {
-          if (C::EARLY) mbar_arrive(B.tok + t);
+          if (TURNS) mbar_arrive(B.tok + t);
         };
-        auto row_max = [&]() {
-          float mx[4];
+        // this row's maximum score of the tile, times the scale; with two
+        // halves, each publishes its own and takes the larger of the two
+        auto row_max = [&](bool& good) -> float {
+          float mx[NC / 32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < NC / 32; ++c) {
             mx[c] = sv[c][0];
 #pragma unroll
             for (int i = 1; i < 31; i += 2) mx[c] = fmax3(mx[c], sv[c][i], sv[c][i + 1]);
             mx[c] = fmaxf(mx[c], sv[c][31]);
           }
-          return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+          float m = mx[0];
+#pragma unroll
+          for (int c = 1; c < NC / 32; ++c) m = fmaxf(m, mx[c]);
+          if (HV == 2) {
+            float* xm = B.xmax + ((g & 1) * 2 + t) * 2 * 128;
+            xm[hf * 128 + r] = m;
+            mbar_arrive(B.xb + 2 * t + (g & 1));
+            good = wait_spin(B.xb + 2 * t + (g & 1), (uint32_t)(g >> 1) & 1u, p.wait_ns);
+            m = fmaxf(m, xm[(hf ^ 1) * 128 + r]);
+          }
+          return m * sc;
         };
-        bool rescale = false;
+        bool rescale = false, xgood = true;
+        if (PWAIT_FIRST && !p_free()) {
+          ok = false;
+          break;
+        }
         if (kt == k0) {
           // first tile of the item: its own max first
-          m_new = row_max();
-          if (!take_turn()) {
+          m_new = row_max(xgood);
+          if (!xgood || !take_turn()) {
             ok = false;
             break;
           }
           lsum = exp_pass(m_new);
           give_turn();
         } else {
-          const float mt = row_max();
+          const float mt = row_max(xgood);
           const bool need = mt > m_run + kRescaleThreshold;
           m_new = need ? mt : m_run;
           alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-          if (!take_turn()) {
+          if (!xgood || !take_turn()) {
             ok = false;
             break;
           }
@@ -727,13 +801,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (rescale) {
           // O may be rescaled only once the previous PV into it has landed
-          if (!mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u)) {
+          if (!mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u, p.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DC / 32; ++c) {
             float tmp[32];
             tmem_ld32(tO + (uint32_t)(c * 32), tmp);
             tmem_wait_ld();
@@ -752,18 +826,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g_last = g - 1;
       if (!ok) break;
       // ---- end of the item's segment: O is complete once the last PV lands
-      if (!mbar_wait(B.o_done + t, (uint32_t)g_last & 1u)) {
+      if (!mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      if (HV == 2) {
+        // the row's sum over both halves' columns
+        float* xs = B.xsum + t * 2 * 128;
+        xs[hf * 128 + r] = l_run;
+        mbar_arrive(B.lb + t);
+        if (!mbar_wait(B.lb + t, (uint32_t)sg & 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        l_run += xs[(hf ^ 1) * 128 + r];
+      }
       u = seg_hi;
       ++sg;
       if (k0 == 0 && k1 == nkt) {
         const float inv = 1.f / l_run;
-        uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
+        uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D + hf * DC;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DC / 32; ++c) {
           float tmp[32];
           load_o(c, tmp);
           if (row < p.q_rows) {
@@ -782,9 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partial: publish (O, m, l) of this row, count in, and merge if last
         const int64_t slot = (item == u_lo / nkt) ? 0 : 1;
         const int64_t rec = ((cta * 2 + slot) * 2 + t) * BM + r;
-        float* wo = p.ws_o + rec * D;
+        float* wo = p.ws_o + rec * D + hf * DC;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DC / 32; ++c) {
           float tmp[32];
           load_o(c, tmp);
 #pragma unroll
@@ -792,58 +877,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             __stcg(reinterpret_cast<float4*>(wo + c * 32 + q),
                    make_float4(tmp[q], tmp[q + 1], tmp[q + 2], tmp[q + 3]));
         }
-        __stcg(p.ws_ml + rec, make_float2(m_run, l_run));
+        if (hf == 0) __stcg(p.ws_ml + rec, make_float2(m_run, l_run));
         __threadfence();
-        const int64_t c_first = sp.owner(item * nkt), c_last = sp.owner((item + 1) * nkt - 1);
-        unsigned int* cnt = p.ws_cnt + (c_first * 2 + t) * BM + r;
-        const unsigned int prev = atomicAdd(cnt, 1u);
-        if (prev == (unsigned int)(c_last - c_first)) {
+        if (HV == 2) {
+          // the row's other half is written too before it is counted
+          mbar_arrive(B.wb + t);
+          if (!mbar_wait(B.wb + t, (uint32_t)nsplit & 1u, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          ++nsplit;
           __threadfence();
-          float M = -INFINITY;
-          for (int64_t cc = c_first; cc <= c_last; ++cc) {
-            const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-            M = fmaxf(M, __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r).x);
-          }
-          float Lsum = 0.f;
-          for (int64_t cc = c_first; cc <= c_last; ++cc) {
-            const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-            const float2 ml = __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r);
-            Lsum += ml.y * fast_exp2(ml.x - M);
-          }
-          const float inv = 1.f / Lsum;
-          uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float acc[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+        }
+        if (hf == 0) {
+          const int64_t c_first = sp.owner(item * nkt), c_last = sp.owner((item + 1) * nkt - 1);
+          unsigned int* cnt = p.ws_cnt + (c_first * 2 + t) * BM + r;
+          const unsigned int prev = atomicAdd(cnt, 1u);
+          if (prev == (unsigned int)(c_last - c_first)) {
+            __threadfence();
+            float M = -INFINITY;
             for (int64_t cc = c_first; cc <= c_last; ++cc) {
               const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-              const int64_t rc = ((cc * 2 + sl) * 2 + t) * BM + r;
-              const float w = fast_exp2(__ldcg(p.ws_ml + rc).x - M) * inv;
-              const float4* src = reinterpret_cast<const float4*>(p.ws_o + rc * D + c * 32);
+              M = fmaxf(M, __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r).x);
+            }
+            float Lsum = 0.f;
+            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+              const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+              const float2 ml = __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r);
+              Lsum += ml.y * fast_exp2(ml.x - M);
+            }
+            const float inv = 1.f / Lsum;
+            uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              float acc[32];
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 v = __ldcg(src + q);
-                acc[4 * q + 0] = __fmaf_rn(v.x, w, acc[4 * q + 0]);
-                acc[4 * q + 1] = __fmaf_rn(v.y, w, acc[4 * q + 1]);
-                acc[4 * q + 2] = __fmaf_rn(v.z, w, acc[4 * q + 2]);
-                acc[4 * q + 3] = __fmaf_rn(v.w, w, acc[4 * q + 3]);
+              for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+              for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+                const int64_t rc = ((cc * 2 + sl) * 2 + t) * BM + r;
+                const float w = fast_exp2(__ldcg(p.ws_ml + rc).x - M) * inv;
+                const float4* src = reinterpret_cast<const float4*>(p.ws_o + rc * D + c * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 v = __ldcg(src + q);
+                  acc[4 * q + 0] = __fmaf_rn(v.x, w, acc[4 * q + 0]);
+                  acc[4 * q + 1] = __fmaf_rn(v.y, w, acc[4 * q + 1]);
+                  acc[4 * q + 2] = __fmaf_rn(v.z, w, acc[4 * q + 2]);
+                  acc[4 * q + 3] = __fmaf_rn(v.w, w, acc[4 * q + 3]);
+                }
+              }
+              if (row < p.q_rows) {
+#pragma unroll
+                for (int q = 0; q < 32; q += 8) {
+                  uint4 pk;
+                  pk.x = pack_bf16x2(acc[q + 0], acc[q + 1]);
+                  pk.y = pack_bf16x2(acc[q + 2], acc[q + 3]);
+                  pk.z = pack_bf16x2(acc[q + 4], acc[q + 5]);
+                  pk.w = pack_bf16x2(acc[q + 6], acc[q + 7]);
+                  *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
+                }
               }
             }
-            if (row < p.q_rows) {
-#pragma unroll
-              for (int q = 0; q < 32; q += 8) {
-                uint4 pk;
-                pk.x = pack_bf16x2(acc[q + 0], acc[q + 1]);
-                pk.y = pack_bf16x2(acc[q + 2], acc[q + 3]);
-                pk.z = pack_bf16x2(acc[q + 4], acc[q + 5]);
-                pk.w = pack_bf16x2(acc[q + 6], acc[q + 7]);
-                *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
-              }
-            }
+            *cnt = 0u;  // ready for the next launch
           }
-          *cnt = 0u;  // ready for the next launch
         }
       }
     }
@@ -856,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < p.S; ++s)
       atomicOr(reinterpret_cast<unsigned long long*>(&p.state[s].pub.error_word),
                (unsigned long long)kErrAttnWaitTimeout);
-  if (wid == 9) {
+  if (wid == C::WI) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -925,7 +1022,7 @@ static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const 
     grid = items;
   }
   if (grid < 1 || grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  attn_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, p);
+  attn_kernel<D><<<(unsigned)grid, Cfg<D>::THREADS, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

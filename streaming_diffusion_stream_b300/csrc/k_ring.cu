@@ -122,39 +122,34 @@ __device__ void copy_frame(const SinkParams& p, int64_t s, int64_t src_row0, int
   }
 }
 
-// grid (blocks, S).  Fill mode copies frames of the chunk into empty sinks.
-// Test mode: every block takes the same decision from the same data (fixed
-// reduction order), copies its share when it fires, and the block that
-// finishes last for the stream updates the embedding and the record -- so
-// no block can read an embedding another block already replaced.
-__global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) {
+// K3a, the decision: grid (S), one block per stream.  Fill mode: the
+// record says which sinks the chunk fills (the copy kernel copies them).
+// Test mode: alpha_j = cos(h, e_j) from exact fp32 products summed as
+// compensated fp32 pairs (fp64 is slow on this part) and a block tree
+// finished in double, j* = argmin (lowest index on ties), fire iff
+// alpha_{j*} < s_th; the record and, on fire, the sink embedding are
+// updated here.  The copy kernel reads the record, so only one block per
+// stream does this work however many blocks copy.
+__global__ void __launch_bounds__(kRingThreads) sink_decide_kernel(const SinkParams p) {
   __shared__ dfloat red[kRingThreads / 32];
   __shared__ double bcast;
   __shared__ int64_t dec_j;
-  __shared__ int last, dec_fire;
-  const int64_t s = blockIdx.y;
+  __shared__ int dec_fire;
+  const int64_t s = blockIdx.x;
   const float* h = p.h + s * p.D;
   DevState* st = p.state + s;
   if (p.fill_from >= 0) {
-    for (int64_t q = 0; q < p.fill_count; ++q) {
-      const int64_t slot = (p.chunk_first + q) % p.R;
-      copy_frame(p, s, (p.M + slot) * p.L, (p.fill_from + q) * p.L);
-    }
-    if (blockIdx.x == 0) {
-      for (int64_t q = 0; q < p.fill_count; ++q)
-        for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x)
-          p.emb[(s * p.M + p.fill_from + q) * p.D + t] = h[t];
-      if (threadIdx.x == 0) {
-        st->pub.sink_j = p.fill_from;
-        st->pub.sink_fire = 2;
-        st->pub.sink_alpha_min = __longlong_as_double(0x7FF0000000000000ll);
-        st->pub.sink_alpha_2 = __longlong_as_double(0x7FF0000000000000ll);
-      }
+    for (int64_t q = 0; q < p.fill_count; ++q)
+      for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x)
+        p.emb[(s * p.M + p.fill_from + q) * p.D + t] = h[t];
+    if (threadIdx.x == 0) {
+      st->pub.sink_j = p.fill_from;
+      st->pub.sink_fire = 2;
+      st->pub.sink_alpha_min = __longlong_as_double(0x7FF0000000000000ll);
+      st->pub.sink_alpha_2 = __longlong_as_double(0x7FF0000000000000ll);
     }
     return;
   }
-  // Each thread sums its exact products as compensated fp32 pairs (fp64 is
-  // slow on this part); the block tree runs in double.
   dfloat hn_t = df_make(0.f);
   for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) hn_t = df_add(hn_t, df_prod(h[t], h[t]));
   const double hn = block_sum_df(hn_t, red, &bcast);
@@ -171,8 +166,6 @@ __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) 
     const double dot = block_sum_df(dot_t, red, &bcast);
     const double en = block_sum_df(en_t, red, &bcast);
     if (threadIdx.x == 0) {
-      // fp64 divide and square root take hundreds of cycles per warp on
-      // this part's narrow fp64 pipe: one thread takes the decision
       const double a = (hn > 0.0 && en > 0.0) ? dot / sqrt(hn * en) : 0.0;
       if (a < amin) {
         a2 = amin;
@@ -186,32 +179,34 @@ __global__ void __launch_bounds__(kRingThreads) sink_kernel(const SinkParams p) 
   if (threadIdx.x == 0) {
     dec_j = jstar;
     dec_fire = amin < p.s_th ? 1 : 0;
-  }
-  __syncthreads();
-  jstar = dec_j;
-  const bool fire = dec_fire != 0;
-  if (fire) {
-    const int64_t slot = p.chunk_first % p.R;
-    copy_frame(p, s, (p.M + slot) * p.L, jstar * p.L);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = (atomicAdd(p.counters + s, 1u) == gridDim.x - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (fire)
-    for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) p.emb[(s * p.M + jstar) * p.D + t] = h[t];
-  if (threadIdx.x == 0) {
     st->pub.sink_j = jstar;
-    st->pub.sink_fire = fire ? 1 : 0;
+    st->pub.sink_fire = dec_fire;
     st->pub.sink_alpha_min = amin;
     st->pub.sink_alpha_2 = a2;
-    p.counters[s] = 0u;
-    __threadfence();
   }
+  __syncthreads();
+  if (dec_fire)
+    for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) p.emb[(s * p.M + dec_j) * p.D + t] = h[t];
+}
+
+// K3b, the copy: grid (blocks, S).  Fill mode copies frames 0.. of the chunk
+// just pushed into the empty sinks; test mode copies frame 0 into sink j*
+// when the decision kernel's record says it fires, and otherwise exits.
+__global__ void __launch_bounds__(kRingThreads) sink_copy_kernel(const SinkParams p) {
+  const int64_t s = blockIdx.y;
+  if (p.fill_from >= 0) {
+    for (int64_t q = 0; q < p.fill_count; ++q) {
+      const int64_t slot = (p.chunk_first + q) % p.R;
+      copy_frame(p, s, (p.M + slot) * p.L, (p.fill_from + q) * p.L);
+    }
+    return;
+  }
+  const DevState* st = p.state + s;
+  if (__ldcg(&st->pub.sink_fire) != 1) return;
+  const int64_t jstar = __ldcg(&st->pub.sink_j);
+  if (jstar < 0 || jstar >= p.M) return;
+  const int64_t slot = p.chunk_first % p.R;
+  copy_frame(p, s, (p.M + slot) * p.L, jstar * p.L);
 }
 
 }  // namespace
@@ -230,13 +225,16 @@ cudaError_t launch_kv_push(const PushParams& p, int sm_count, cudaStream_t st) {
 }
 
 cudaError_t launch_sink_refresh(const SinkParams& p, int sm_count, cudaStream_t st) {
+  sink_decide_kernel<<<(unsigned)p.S, kRingThreads, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int64_t vecs = p.L * (p.HD / 8);
   int64_t bx = (vecs + kRingThreads - 1) / kRingThreads;
   int64_t cap = ((int64_t)sm_count * 4 + p.S - 1) / p.S;
   if (bx > cap) bx = cap;
   if (bx < 1) bx = 1;
   dim3 grid((unsigned)bx, (unsigned)p.S);
-  sink_kernel<<<grid, kRingThreads, 0, st>>>(p);
+  sink_copy_kernel<<<grid, kRingThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 
