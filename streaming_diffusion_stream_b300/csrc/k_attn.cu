@@ -88,7 +88,17 @@ struct Cfg {
   // O0 [384,448) O1 [448,512).  d = 128 has no spare columns: P overwrites
   // the first 64 columns of its S and one thread issues every MMA.
   static constexpr bool EARLY = (D == 64);
-  static constexpr int ISS = EARLY ? 2 : 1;  // MMA-issuing threads
+#ifndef SDS_K1_ISS128
+#define SDS_K1_ISS128 1
+#endif
+  // MMA-issuing threads.  One thread issues an MMA about every 100 cycles
+  // under load against 64 cycles of tensor work for M128 N128 K16, so a
+  // single issuer cannot keep the tensor core busy; with two, issuer t
+  // serves query tile t alone.  d = 128 keeps P over the scores, so there
+  // issuer t issues PV_t(g) before S_t(g+1) (one thread's MMAs run in issue
+  // order, so S_t(g+1) cannot overwrite P_t(g) before PV_t(g) has read it).
+  static constexpr int ISS = EARLY ? 2 : SDS_K1_ISS128;
+  static constexpr bool PV_FIRST = !EARLY;  // always PV_t(g) before S_t(g+1)
   static constexpr uint32_t O_COL = EARLY ? 384u : 256u;  // first column of O0
   static constexpr uint32_t O_STRIDE = EARLY ? 64u : 128u;
   // Threads per query row (HV, "halves"): with two, each of the two threads
@@ -104,13 +114,28 @@ struct Cfg {
 #define SDS_K1_TURNS 1
 #endif
 #ifndef SDS_K1_PWAIT_FIRST
-#define SDS_K1_PWAIT_FIRST 1
+#define SDS_K1_PWAIT_FIRST 0
 #endif
-  static constexpr int HV = (D == 64) ? SDS_K1_HV64 : 1;
+#ifndef SDS_K1_HV128
+#define SDS_K1_HV128 1
+#endif
+#ifndef SDS_K1_CHAINS
+#define SDS_K1_CHAINS 4
+#endif
+  static constexpr int HV = (D == 64) ? SDS_K1_HV64 : SDS_K1_HV128;
   static constexpr int SMW = 8 * HV;              // softmax warps (two tiles)
-  static constexpr int WP = SMW;                  // TMA producer warp
+#ifndef SDS_K1_SPLITV
+#define SDS_K1_SPLITV 0
+#endif
+  // K (with Q) and V tiles come from separate producer warps, so that a
+  // producer waiting for a free V stage (held until the PV products of two
+  // tiles back are done) does not hold back the next K tile, which the
+  // next S product needs earlier.
+  static constexpr bool SPLITV = SDS_K1_SPLITV;
+  static constexpr int WP = SMW;                  // TMA producer warp (K, Q; and V unless SPLITV)
   static constexpr int WI = SMW + 1;              // MMA issuer warp(s): WI, WI + 1
-  static constexpr int THREADS = (SMW + 3) * 32;  // softmax + producer + 2 issuer warps
+  static constexpr int WPV = SMW + 3;             // V producer warp (SPLITV)
+  static constexpr int THREADS = (SMW + (SPLITV ? 4 : 3)) * 32;
   static constexpr int Q = 0;
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
@@ -291,14 +316,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     prefetch_tensormap(&tm_v);
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.q_full + i, 1);
-      mbar_init(B.q_empty + i, C::EARLY ? 2 : 1);
+      mbar_init(B.q_empty + i, C::ISS);
       mbar_init(B.q_ready + 2 * i + 0, 128 * C::HV);
       mbar_init(B.q_ready + 2 * i + 1, 128 * C::HV);
     }
     for (int i = 0; i < C::ST; ++i) {
       mbar_init(B.k_full + i, 1);
       mbar_init(B.v_full + i, 1);
-      mbar_init(B.k_empty + i, C::EARLY ? 2 : 1);
+      mbar_init(B.k_empty + i, C::ISS);
       mbar_init(B.v_empty + i, C::ISS);
     }
     for (int i = 0; i < 2; ++i) {
@@ -325,8 +350,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *B.tmem_slot;
 
-  if (wid == C::WP) {
-    // ------------------------------------------------------------ TMA producer
+  if (wid == C::WP || (C::SPLITV && wid == C::WPV)) {
+    // ------------------------------------------------------------ TMA producer(s)
+    const bool do_k = wid == C::WP;                  // K and Q
+    const bool do_v = !C::SPLITV || wid == C::WPV;   // V
     if (lane == 0 && active) {
       SegIter it;
       it.init(u_lo, u_hi, nkt);
@@ -340,22 +367,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const ItemPos ip = item_pos(p, it.item, npairs);
         int key0, nvalid;
         key_tile(p, nt0, it.kt(), key0, nvalid);
-        if (!mbar_wait(B.k_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
-        // failure-detection test hook: CTA 0 never loads the keys of tile
-        // `withhold_k`, so every wait for them runs out
-        const bool withhold = p.withhold_k >= 0 && g == p.withhold_k && cta == 0;
-        if (!withhold) {
-          mbar_arrive_expect_tx(B.k_full + st, C::TILE);
-          for (int b = 0; b < C::NSUB; ++b)
-            tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, ip.h * D + b * 64, key0, ip.s, B.k_full + st);
+        if (do_k) {
+          if (!mbar_wait(B.k_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
+          // failure-detection test hook: CTA 0 never loads the keys of tile
+          // `withhold_k`, so every wait for them runs out
+          const bool withhold = p.withhold_k >= 0 && g == p.withhold_k && cta == 0;
+          if (!withhold) {
+            mbar_arrive_expect_tx(B.k_full + st, C::TILE);
+            for (int b = 0; b < C::NSUB; ++b)
+              tma_load_3d(sK + st * C::TILE + b * SUB, &tm_k, ip.h * D + b * 64, key0, ip.s, B.k_full + st);
+          }
+          issued_k = g + 1;
         }
-        issued_k = g + 1;
-        if (!mbar_wait(B.v_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
-        mbar_arrive_expect_tx(B.v_full + st, C::TILE);
-        for (int b = 0; b < C::NSUB; ++b)
-          tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
-        issued_v = g + 1;
-        if (it.first()) {
+        if (do_v) {
+          if (!mbar_wait(B.v_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
+          mbar_arrive_expect_tx(B.v_full + st, C::TILE);
+          for (int b = 0; b < C::NSUB; ++b)
+            tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
+          issued_v = g + 1;
+        }
+        if (do_k && it.first()) {
           // this item's queries; the buffer is free once the last S MMAs
           // of the item that used it before have completed
           const int qb = it.sg % C::QB;
@@ -381,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
         mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u, p.wait_ns);
     }
-  } else if (C::EARLY && (wid == C::WI || wid == C::WI + 1)) {
+  } else if (C::ISS == 2 && (wid == C::WI || wid == C::WI + 1)) {
     // ------------------------------------------------------------ MMA issuers (d = 64):
     // one thread per query tile t, for S_t = Q_t K^T and O_t += P_t V.
     // S_t(g+1) goes out as soon as the softmax has read S_t(g) (s_free) and
@@ -396,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const uint32_t klo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
       const uint32_t dS = tmem + (uint32_t)(t * 128);
-      const uint32_t aP = tmem + 256u + (uint32_t)(t * 64);
+      const uint32_t aP = C::EARLY ? tmem + 256u + (uint32_t)(t * 64) : tmem + (uint32_t)(t * 128);
       const uint32_t dO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE;
       auto issue_s = [&](int qb, uint32_t st) {
         const uint32_t a0 = qlo + (uint32_t)(((qb * 2 + t) * C::TILE) >> 4);
@@ -449,7 +480,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           // at a boundary S_t(g+1) goes after PV_t(g)
           auto next_s = [&]() -> bool {
             const int qb1 = boundary ? qb_n : sg % C::QB;
-            if (!mbar_wait(B.k_full + st1, ph1, p.wait_ns) || !mbar_wait(B.s_free + t, g & 1u, p.wait_ns) ||
+            if (!mbar_wait(B.k_full + st1, ph1, p.wait_ns) ||
+                (C::EARLY && !mbar_wait(B.s_free + t, g & 1u, p.wait_ns)) ||
                 (boundary && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n, p.wait_ns)))
               return false;
             tc_fence_after();
@@ -459,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             if (next_last) mma_commit(B.q_empty + qb1);
             return true;
           };
-          if (more && !boundary && !next_s()) {
+          if (more && !boundary && !C::PV_FIRST && !next_s()) {
             ok = false;
             break;
           }
@@ -471,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           issue_pv(st, i > 0);
           mma_commit(B.o_done + t);
           mma_commit(B.v_empty + st);
-          if (more && boundary && !next_s()) {
+          if (more && (boundary || C::PV_FIRST) && !next_s()) {
             ok = false;
             break;
           }
@@ -483,7 +515,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mma_commit(B.mma_final + t);
       mbar_wait(B.mma_final + t, 0, p.wait_ns);
     }
-  } else if (wid == C::WI) {
+  } else if (C::ISS == 1 && wid == C::WI) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && active) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
@@ -710,8 +742,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         bool pwait_ok = true;
         auto exp_pass = [&](float m) -> float {
           const float2 nm2 = make_float2(-m, -m);
-          float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
+          constexpr int NRS = SDS_K1_CHAINS;  // independent row-sum chains
+          float2 rs[NRS];
+#pragma unroll
+          for (int i = 0; i < NRS; ++i) rs[i] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int part = 0; part < NPART; ++part) {
 #pragma unroll
@@ -719,7 +753,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
               const float a0 = sv[part][2 * q], a1 = sv[part][2 * q + 1];
               const float2 x = __ffma2_rn(make_float2(a0, a1), sc2, nm2);
               const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
-              rs[q & 3] = __fadd2_rn(rs[q & 3], make_float2(e0, e1));
+              rs[q % NRS] = __fadd2_rn(rs[q % NRS], make_float2(e0, e1));
               pk[part][q] = pack_bf16x2(e0, e1);
             }
             if (part >= HOLD) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
@@ -729,8 +763,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
               for (int h = 0; h < HOLD; ++h) tmem_st16u(tP + (uint32_t)(h * 16), pk[h]);
             }
           }
-          const float2 s01 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-          return s01.x + s01.y;
+#pragma unroll
+          for (int w2 = NRS / 2; w2 > 0; w2 /= 2)
+#pragma unroll
+            for (int i = 0; i < w2; ++i) rs[i] = __fadd2_rn(rs[i], rs[i + w2]);
+          return rs[0].x + rs[0].y;
         };
         float alpha = 1.f, m_new, lsum;
         // EARLY with one thread per row: the two groups take turns at the
@@ -748,17 +785,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // this row's maximum score of the tile, times the scale; with two
         // halves, each publishes its own and takes the larger of the two
         auto row_max = [&](bool& good) -> float {
-          float mx[NC / 32];
+          // SPL independent chains per 32 columns
+          constexpr int SPL = (SDS_K1_CHAINS > 4 && NC == 128) || (SDS_K1_CHAINS > 2 && NC == 64) ? 2 : 1;
+          constexpr int LEN = 32 / SPL;
+          float mx[NC / 32][SPL];
 #pragma unroll
-          for (int c = 0; c < NC / 32; ++c) {
-            mx[c] = sv[c][0];
+          for (int c = 0; c < NC / 32; ++c)
 #pragma unroll
-            for (int i = 1; i < 31; i += 2) mx[c] = fmax3(mx[c], sv[c][i], sv[c][i + 1]);
-            mx[c] = fmaxf(mx[c], sv[c][31]);
-          }
-          float m = mx[0];
+            for (int h = 0; h < SPL; ++h) {
+              const int b0 = h * LEN;
+              float v = fmax3(sv[c][b0], sv[c][b0 + 1], sv[c][b0 + 2]);
 #pragma unroll
-          for (int c = 1; c < NC / 32; ++c) m = fmaxf(m, mx[c]);
+              for (int i = b0 + 3; i + 1 < b0 + LEN; i += 2) v = fmax3(v, sv[c][i], sv[c][i + 1]);
+              if ((LEN - 3) % 2) v = fmaxf(v, sv[c][b0 + LEN - 1]);
+              mx[c][h] = v;
+            }
+          float m = mx[0][0];
+#pragma unroll
+          for (int c = 0; c < NC / 32; ++c)
+#pragma unroll
+            for (int h = 0; h < SPL; ++h)
+              if (c + h > 0) m = fmaxf(m, mx[c][h]);
           if (HV == 2) {
             float* xm = B.xmax + ((g & 1) * 2 + t) * 2 * 128;
             xm[hf * 128 + r] = m;

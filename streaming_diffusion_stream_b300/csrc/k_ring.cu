@@ -16,6 +16,7 @@ namespace sds {
 namespace {
 
 constexpr int kRingThreads = 256;
+constexpr int kDecideThreads = 512;  // one block per stream takes the sink decision
 constexpr int kPushX = 64;  // threads along a token row (a multiple of head_dim / 8)
 constexpr int kPushY = 4;   // token rows per block
 
@@ -90,7 +91,7 @@ __device__ double block_sum_df(dfloat v, dfloat* red, double* out) {
   __syncthreads();
   if (threadIdx.x == 0) {
     dfloat t = red[0];
-    for (int w = 1; w < kRingThreads / 32; ++w) t = df_add(t, red[w]);
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = df_add(t, red[w]);
     *out = df_to_double(t);
   }
   __syncthreads();
@@ -130,8 +131,8 @@ __device__ void copy_frame(const SinkParams& p, int64_t s, int64_t src_row0, int
 // alpha_{j*} < s_th; the record and, on fire, the sink embedding are
 // updated here.  The copy kernel reads the record, so only one block per
 // stream does this work however many blocks copy.
-__global__ void __launch_bounds__(kRingThreads) sink_decide_kernel(const SinkParams p) {
-  __shared__ dfloat red[kRingThreads / 32];
+__global__ void __launch_bounds__(kDecideThreads) sink_decide_kernel(const SinkParams p) {
+  __shared__ dfloat red[kDecideThreads / 32];
   __shared__ double bcast;
   __shared__ int64_t dec_j;
   __shared__ int dec_fire;
@@ -150,19 +151,57 @@ __global__ void __launch_bounds__(kRingThreads) sink_decide_kernel(const SinkPar
     }
     return;
   }
-  dfloat hn_t = df_make(0.f);
-  for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) hn_t = df_add(hn_t, df_prod(h[t], h[t]));
-  const double hn = block_sum_df(hn_t, red, &bcast);
+  // One pass per sink over h and e_j: dot_j = h.e_j, en_j = e_j.e_j, and,
+  // with the first sink, hn = h.h.  Each thread takes 4 consecutive
+  // elements per step and issues the loads of two steps before it uses them,
+  // so the memory round trips overlap instead of following each other.
+  const bool vec = (p.D % 4 == 0) && ((reinterpret_cast<uintptr_t>(h) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(p.emb) & 15u) == 0);
+  double hn = 0.0;
   int64_t jstar = -1;
   double amin = __longlong_as_double(0x7FF0000000000000ll), a2 = amin;
   for (int64_t j = 0; j < p.M; ++j) {
     const float* e = p.emb + (s * p.M + j) * p.D;
-    dfloat dot_t = df_make(0.f), en_t = df_make(0.f);
-    for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) {
-      const float ev = e[t];
-      dot_t = df_add(dot_t, df_prod(h[t], ev));
-      en_t = df_add(en_t, df_prod(ev, ev));
+    dfloat dot_t = df_make(0.f), en_t = df_make(0.f), hn_t = df_make(0.f);
+    const bool with_hn = j == 0;
+    if (vec) {
+      const int64_t stride = (int64_t)blockDim.x * 4;
+      int64_t t = (int64_t)threadIdx.x * 4;
+      for (; t + stride < p.D; t += 2 * stride) {
+        const float4 h0 = __ldg(reinterpret_cast<const float4*>(h + t));
+        const float4 e0 = __ldcg(reinterpret_cast<const float4*>(e + t));
+        const float4 h1 = __ldg(reinterpret_cast<const float4*>(h + t + stride));
+        const float4 e1 = __ldcg(reinterpret_cast<const float4*>(e + t + stride));
+        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          dot_t = df_add(dot_t, df_prod(hv[q], ev[q]));
+          en_t = df_add(en_t, df_prod(ev[q], ev[q]));
+          if (with_hn) hn_t = df_add(hn_t, df_prod(hv[q], hv[q]));
+        }
+      }
+      if (t < p.D) {
+        const float4 h0 = __ldg(reinterpret_cast<const float4*>(h + t));
+        const float4 e0 = __ldcg(reinterpret_cast<const float4*>(e + t));
+        const float hv[4] = {h0.x, h0.y, h0.z, h0.w};
+        const float ev[4] = {e0.x, e0.y, e0.z, e0.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dot_t = df_add(dot_t, df_prod(hv[q], ev[q]));
+          en_t = df_add(en_t, df_prod(ev[q], ev[q]));
+          if (with_hn) hn_t = df_add(hn_t, df_prod(hv[q], hv[q]));
+        }
+      }
+    } else {
+      for (int64_t t = threadIdx.x; t < p.D; t += blockDim.x) {
+        const float hv = h[t], ev = e[t];
+        dot_t = df_add(dot_t, df_prod(hv, ev));
+        en_t = df_add(en_t, df_prod(ev, ev));
+        if (with_hn) hn_t = df_add(hn_t, df_prod(hv, hv));
+      }
     }
+    if (with_hn) hn = block_sum_df(hn_t, red, &bcast);
     const double dot = block_sum_df(dot_t, red, &bcast);
     const double en = block_sum_df(en_t, red, &bcast);
     if (threadIdx.x == 0) {
@@ -225,7 +264,7 @@ cudaError_t launch_kv_push(const PushParams& p, int sm_count, cudaStream_t st) {
 }
 
 cudaError_t launch_sink_refresh(const SinkParams& p, int sm_count, cudaStream_t st) {
-  sink_decide_kernel<<<(unsigned)p.S, kRingThreads, 0, st>>>(p);
+  sink_decide_kernel<<<(unsigned)p.S, kDecideThreads, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t vecs = p.L * (p.HD / 8);

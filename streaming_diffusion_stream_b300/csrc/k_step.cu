@@ -428,7 +428,12 @@ cudaError_t launch_step(const StepParams& p, int sm_count, cudaStream_t st) {
   const int64_t tot = (p.n > 0 ? p.S * p.nb_u : 0) + (p.ssf_frame ? p.S * p.nb_s : 0) +
                       (p.mot_chunk ? p.S * p.T * p.nb_m : 0);
   if (tot == 0) return cudaSuccess;
-  const int64_t cap = (int64_t)sm_count * (2048 / kStepThreads);
+#ifndef SDS_K4_BLOCKS_PER_SM
+#define SDS_K4_BLOCKS_PER_SM 8
+#endif
+  // A resident grid (SDS_K4_BLOCKS_PER_SM blocks per SM) strides over the
+  // work units.
+  const int64_t cap = (int64_t)sm_count * SDS_K4_BLOCKS_PER_SM;
   const int grid = (int)(tot < cap ? tot : cap);
   switch (p.n) {
     case 0:
