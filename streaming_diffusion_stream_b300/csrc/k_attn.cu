@@ -111,7 +111,7 @@ struct Cfg {
 #define SDS_K1_HV64 1
 #endif
 #ifndef SDS_K1_TURNS
-#define SDS_K1_TURNS 1
+#define SDS_K1_TURNS 2
 #endif
 #ifndef SDS_K1_PWAIT_FIRST
 #define SDS_K1_PWAIT_FIRST 0
@@ -173,6 +173,7 @@ struct Bars {
   uint64_t* xb;         // [2 tile][2 parity]: both halves' row maxima are in shared memory (HV 2)
   uint64_t* lb;         // [2 tile]: both halves' row sums are in shared memory (HV 2)
   uint64_t* wb;         // [2 tile]: both halves' partial O rows are written (HV 2, split items)
+  uint64_t* tokw;       // [2 group][2 half][4 sub-partition]: per-warp turns at the exponentials
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   float* xmax;          // [2 parity][2 tile][2 half][128]
@@ -200,7 +201,8 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.xb = r.tok + 2;
   r.lb = r.xb + 4;
   r.wb = r.lb + 2;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(r.wb + 2);
+  r.tokw = r.wb + 2;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.tokw + 16);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   r.xmax = reinterpret_cast<float*>(sm + C::XCH);
   r.xsum = r.xmax + 8 * 128;
@@ -338,6 +340,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(B.lb + i, 128 * C::HV);
       mbar_init(B.wb + i, 128 * C::HV);
     }
+    for (int i = 0; i < 16; ++i) mbar_init(B.tokw + i, 32);
     *B.abort_flag = 0;
     fence_barrier_init();
   }
@@ -738,6 +741,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // P waits in registers and the wait falls in the middle.
         constexpr bool PWAIT_FIRST = C::EARLY && SDS_K1_PWAIT_FIRST;
         constexpr int HOLD = (C::EARLY && !PWAIT_FIRST) ? NPART / 2 : 0;  // parts held until P is free
+        // SDS_K1_TURNS 2: the turn passes between the two warps that share
+        // an SM sub-partition (warp w of group 0 and warp w + 4 of group 1),
+        // each pair on its own, since each sub-partition has its own
+        // exponential unit.  SDS_K1_TURNS 3: the same, with each warp's
+        // exponentials in two halves around its wait for PV(g-1), so that
+        // the other warp's half runs on the unit during that wait
+        // (G0 first, G1 first, G0 second, G1 second, then the next tile).
+        constexpr bool TURNS = C::EARLY && SDS_K1_TURNS;
+        constexpr bool WTURNS = TURNS && SDS_K1_TURNS >= 2 && HV == 1;
+        constexpr bool HTURNS = WTURNS && SDS_K1_TURNS == 3 && HOLD > 0;
+        const int sp4 = wid & 3;
+        // barrier of group tt, half hh, this sub-partition
+        auto tokw = [&](int tt, int hh) { return B.tokw + (tt * 2 + hh) * 4 + sp4; };
+        auto take_half = [&](int hh) -> bool {
+          if (t == 0) {
+            if (hh == 0) return g == 0 || wait_spin(tokw(1, 1), (uint32_t)(g - 1) & 1u, p.wait_ns);
+            return wait_spin(tokw(1, 0), (uint32_t)g & 1u, p.wait_ns);
+          }
+          return wait_spin(tokw(0, hh), (uint32_t)g & 1u, p.wait_ns);
+        };
+        auto take_turn = [&]() -> bool {
+          if (!TURNS) return true;
+          if (HTURNS) return take_half(0);
+          if (WTURNS) {
+            if (t == 0) return g == 0 || wait_spin(tokw(1, 0), (uint32_t)(g - 1) & 1u, p.wait_ns);
+            return wait_spin(tokw(0, 0), (uint32_t)g & 1u, p.wait_ns);
+          }
+          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u, p.wait_ns);
+          return wait_spin(B.tok + 0, (uint32_t)g & 1u, p.wait_ns);
+        };
+        auto give_turn = [&]() {
+          if (HTURNS) {
+            mbar_arrive(tokw(t, 1));
+          } else if (WTURNS) {
+            mbar_arrive(tokw(t, 0));
+          } else if (TURNS) {
+            mbar_arrive(B.tok + t);
+          }
+        };
         uint32_t pk[NPART][16];
         bool pwait_ok = true;
         auto exp_pass = [&](float m) -> float {
@@ -758,7 +800,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             }
             if (part >= HOLD) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
             if (HOLD > 0 && part == HOLD - 1) {
+              if (HTURNS) mbar_arrive(tokw(t, 0));  // first half done: the partner's turn
               pwait_ok = p_free();
+              if (HTURNS) pwait_ok = take_half(1) && pwait_ok;
 #pragma unroll
               for (int h = 0; h < HOLD; ++h) tmem_st16u(tP + (uint32_t)(h * 16), pk[h]);
             }
@@ -773,15 +817,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // EARLY with one thread per row: the two groups take turns at the
         // exponentials (E0(g), E1(g), E0(g+1), ...), so each runs alone on
         // the MUFU pipe while the other loads scores and takes its row max
-        constexpr bool TURNS = C::EARLY && SDS_K1_TURNS;
-        auto take_turn = [&]() -> bool {
-          if (!TURNS) return true;
-          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u, p.wait_ns);
-          return wait_spin(B.tok + 0, (uint32_t)g & 1u, p.wait_ns);
-        };
-        auto give_turn = [&]() {
-          if (TURNS) mbar_arrive(B.tok + t);
-        };
         // this row's maximum score of the tile, times the scale; with two
         // halves, each publishes its own and takes the larger of the two
         auto row_max = [&](bool& good) -> float {
