@@ -20,42 +20,45 @@
 // Warp roles inside a CTA:
 //   warps 0-3  softmax group 0 (tile Q0), one query row per thread = one TMEM lane
 //   warps 4-7  softmax group 1 (tile Q1)
-//   warp  8    TMA producer: K and V tiles through an ST-stage ring, Q per item
-//   warp  9    MMA issuer (one thread): tcgen05.mma into tensor memory
-//   warp  10   d = 64 only: the second MMA issuer
-// d = 128.  Tensor memory (512 columns): S0 [0,128), S1 [128,256) fp32
-// scores; O0 [256,384), O1 [384,512) fp32 accumulators.  Each group writes
-// its probabilities P as packed bf16 over the first 64 columns of its own S
-// region, and O += P V reads P straight from tensor memory (A operand in
-// TMEM), so P never touches shared memory.  The one issuer interleaves
-//   PV0(g), S0(g+1), PV1(g), S1(g+1), ...
-// so the tensor core works on one group's tile while the other group runs
-// its softmax (ping-pong); tcgen05 MMAs from one thread run in issue order,
-// so S_t(g+1) may overwrite the P_t(g) columns that PV_t(g) reads.
-// d = 64.  The tensor work of a tile is half as long, so ping-pong alone
-// leaves the tensor core idle while a group's softmax runs.  P_t gets
-// columns of its own (S0, S1, P0, P1, O0, O1 = 128+128+64+64+64+64), and
-// issuer t serves tile t alone: it issues S_t(g+1) as soon as group t has
-// read S_t(g) into registers (s_free), then PV_t(g) once P_t(g) is written,
-// so the next scores are ready when the softmax finishes the current tile.
-// Group t writes P_t(g) only after PV_t(g-1) has completed; it waits for
-// that halfway through its exponentials, holding the first half of P in
-// registers.  The two groups take turns at the exponentials (E0(g), E1(g),
-// E0(g+1), ...): each then has the MUFU pipe to itself while the other
-// loads its scores and takes its row max.  At an item boundary PV_t(g) is issued before S_t(g+1),
-// because the next item's queries are rotated by the softmax only once it
-// has finished the current item.
+//   warp  8    TMA producer: K and V tiles of 128 keys through an ST-stage ring, Q per item
+//   warps 9-10 MMA issuers (one thread each): issuer t serves query tile t
+// d = 64.  Tensor memory (512 columns): S0, S1 (128 each, fp32 scores),
+// P0, P1 (64 each, packed bf16), O0, O1 (64 each).  Issuer t issues S_t(g+1)
+// as soon as group t has read S_t(g) into registers (s_free), then PV_t(g)
+// once P_t(g) is written, so the next scores are ready when the softmax
+// finishes the current tile.  Group t writes P_t(g) only after PV_t(g-1)
+// has completed; it waits for that halfway through its exponentials,
+// holding the first half of P in registers.  The exponentials of the two
+// groups take turns on each SM sub-partition: warp w of group 0 and warp
+// w + 4 of group 1 share one, and hand the turn to each other pair by pair,
+// so each runs alone on its sub-partition's exponential unit while the
+// other loads its scores and takes its row max.  At an item boundary
+// PV_t(g) is issued before S_t(g+1), because the next item's queries are
+// rotated by the softmax only once it has finished the current item.
+// d = 128.  Each loaded key tile is consumed as two 64-key compute tiles.
+// Tensor memory per group t: two score buffers [t*256, +64), [t*256 + 64,
+// +64) and O_t [t*256 + 128, +128).  P_t(g) is written over the first 32
+// columns of its score buffer; issuer t issues PV_t(g) and then S_t(g+2)
+// into the same buffer (one thread's MMAs run in issue order, so the PV
+// reads P before the S overwrites it), keeping the scores of the next
+// compute tile ready while the softmax works on the current one.  Each
+// score buffer has its own s_full / p_full barriers, so that no barrier can
+// run two phases ahead of its waiter (a parity wait distinguishes only the
+// current and the previous phase).
 // In both cases the waits for K/V data, which the producer lands several
 // tiles ahead, are taken before the wait for P so they stay off the
 // critical path.
 // The online softmax keeps a running max m per row and rescales O (in
 // tensor memory) only when a tile raises m by more than 8 (log2 units):
-// otherwise probabilities may exceed 1 by up to 2^8, which fp32 sums and bf16
-// P hold without loss.  Each tile's row max is taken first (a three-input
-// max); the exponentials go against the running max unless the tile raises
-// it past the threshold.  Score scaling and row sums use packed f32x2
-// arithmetic, halving their instruction count.  Every wait has a time limit; on expiry the kernel records
+// otherwise probabilities may exceed 1 by up to 2^8, which fp32 sums and
+// bf16 P hold without loss.  Each tile's row max is taken first (a
+// three-input max); the exponentials go against the running max unless the
+// tile raises it past the threshold.  Score scaling and row sums use packed
+// f32x2 arithmetic, halving their instruction count.  Every wait has a time
+// limit (the launch's wait_ns); on expiry the kernel records
 // kErrAttnWaitTimeout in the error word of every stream and leaves.
+// The schedule knobs (SDS_K1_*) select measured alternatives of the same
+// computation; their defaults are the fastest measured on a B300.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -97,10 +100,24 @@ struct Cfg {
   // serves query tile t alone.  d = 128 keeps P over the scores, so there
   // issuer t issues PV_t(g) before S_t(g+1) (one thread's MMAs run in issue
   // order, so S_t(g+1) cannot overwrite P_t(g) before PV_t(g) has read it).
-  static constexpr int ISS = EARLY ? 2 : SDS_K1_ISS128;
+#ifndef SDS_K1_SUB64
+#define SDS_K1_SUB64 1
+#endif
+  // d = 128 with 64-key compute tiles (SUBS = 2): each loaded 128-key tile
+  // is consumed as two 64-key halves.  Tensor memory then holds two score
+  // buffers per group, [t*256, +64) and [t*256 + 64, +64), beside O_t at
+  // [t*256 + 128, +128): the issuer of group t computes S_t(g+2) into the
+  // buffer of S_t(g) right after PV_t(g) has read the P written over it,
+  // so the scores of the next half-tile are ready while the softmax works
+  // on the current one, and the group's tensor work never waits for its
+  // own softmax.
+  static constexpr int SUBS = (D == 128 && SDS_K1_SUB64) ? 2 : 1;
+  static constexpr int NCOL = BN / SUBS;  // keys per compute tile
+  static constexpr int ISS = (EARLY || SUBS == 2) ? 2 : SDS_K1_ISS128;
   static constexpr bool PV_FIRST = !EARLY;  // always PV_t(g) before S_t(g+1)
-  static constexpr uint32_t O_COL = EARLY ? 384u : 256u;  // first column of O0
-  static constexpr uint32_t O_STRIDE = EARLY ? 64u : 128u;
+  static constexpr uint32_t O_COL = EARLY ? 384u : (SUBS == 2 ? 128u : 256u);  // first column of O0
+  static constexpr uint32_t O_STRIDE = EARLY ? 64u : (SUBS == 2 ? 256u : 128u);
+  static constexpr uint32_t S_STRIDE = SUBS == 2 ? 256u : 128u;  // S region of group t at t * S_STRIDE
   // Threads per query row (HV, "halves"): with two, each of the two threads
   // of a row takes half of its score columns, P columns and O columns, so
   // that a tile has 8 softmax warps (2 per SM sub-partition and tile) and the
@@ -140,7 +157,7 @@ struct Cfg {
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
   static constexpr int BAR = V + ST * TILE;
-  static constexpr int XCH = BAR + 512;           // row-max [2 parity][2 tile][2 half][128], row-sum [2][2][128]
+  static constexpr int XCH = BAR + 640;           // row-max [2 parity][2 tile][2 half][128], row-sum [2][2][128]
   static constexpr int TOTAL = XCH + (HV == 2 ? (8 + 4) * 128 * 4 : 0);
   static constexpr int ALLOC = TOTAL + 1024;  // slack for 1024-byte alignment
 };
@@ -164,8 +181,8 @@ struct Bars {
   uint64_t* v_full;
   uint64_t* k_empty;
   uint64_t* v_empty;
-  uint64_t* s_full;  // [2]
-  uint64_t* p_full;  // [2]
+  uint64_t* s_full;  // [2 group][2 buffer]: index t, or t * 2 + buffer with 64-key compute tiles
+  uint64_t* p_full;  // [2 group][2 buffer], indexed as s_full
   uint64_t* o_done;  // [2]
   uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
@@ -193,8 +210,8 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.k_empty = r.v_full + C::ST;
   r.v_empty = r.k_empty + C::ST;
   r.s_full = r.v_empty + C::ST;
-  r.p_full = r.s_full + 2;
-  r.o_done = r.p_full + 2;
+  r.p_full = r.s_full + 4;
+  r.o_done = r.p_full + 4;
   r.mma_final = r.o_done + 2;
   r.s_free = r.mma_final + 2;
   r.tok = r.s_free + 2;
@@ -328,9 +345,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(B.k_empty + i, C::ISS);
       mbar_init(B.v_empty + i, C::ISS);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(B.s_full + i, 1);
       mbar_init(B.p_full + i, 128 * C::HV);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(B.o_done + i, 1);
       mbar_init(B.mma_final + i, 1);
       mbar_init(B.s_free + i, 128 * C::HV);
@@ -415,7 +434,133 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
         mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u, p.wait_ns);
     }
-  } else if (C::ISS == 2 && (wid == C::WI || wid == C::WI + 1)) {
+  } else if (C::SUBS == 2 && (wid == C::WI || wid == C::WI + 1)) {
+    // ------------------------------------------------------------ MMA issuers (d = 128,
+    // 64-key compute tiles): issuer t serves query tile t.  The two halves
+    // h of a loaded key tile have score buffers of their own; once PV_t(g)
+    // has been issued, S_t(g + 2) goes into the same buffer (one thread's
+    // MMAs run in issue order, so PV_t(g) reads the P written over the
+    // scores before S_t(g + 2) overwrites them).  At an item boundary the
+    // next item's two S products follow the item's last PV, because the
+    // softmax rotates the next item's queries only once it has finished
+    // the item.
+    if (lane == 0 && active) {
+      const int t = wid - C::WI;
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, C::NCOL, false);
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
+      const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
+      const uint32_t qlo = (uint32_t)smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t klo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
+      const uint32_t dS = tmem + (uint32_t)t * C::S_STRIDE;  // buffer h at dS + h * NCOL
+      const uint32_t dO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE;
+      // S_t of half h of the K tile in stage st: keys [h * NCOL, +NCOL) are
+      // rows h * NCOL.. of each 64-column sub-tile (a multiple of the 8-row
+      // swizzle atom, so the descriptor only moves its start address)
+      auto issue_s = [&](int qb, uint32_t st, int h) {
+        const uint32_t a0 = qlo + (uint32_t)(((qb * 2 + t) * C::TILE) >> 4);
+        const uint32_t b0 = klo + st * (uint32_t)(C::TILE >> 4) + (uint32_t)((h * C::NCOL * 128) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(((kk >> 2) * SUB + (kk & 3) * 32) >> 4);
+          mma_bf16_ss_w(dS + (uint32_t)(h * C::NCOL), a0 + off, dhi, b0 + off, dhi, IDESC_S,
+                        kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t(half h) V(rows h * NCOL.. of the V tile in stage st)
+      auto issue_pv = [&](uint32_t st, int h, bool acc) {
+        const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
+        const uint32_t aP = dS + (uint32_t)(h * C::NCOL);
+#pragma unroll
+        for (int kk = 0; kk < C::NCOL / 16; ++kk)
+          mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8),
+                        b0 + (uint32_t)(((h * C::NCOL + kk * 16) * 128) >> 4), dhi, IDESC_O,
+                        (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      uint32_t L = 0;  // loaded key tiles consumed (compute tiles 2L, 2L + 1)
+      int sg = 0;      // segment counter
+      int64_t u = u_lo;
+      {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        ok = mbar_wait(B.q_ready + t, 0, p.wait_ns) && mbar_wait(B.k_full, 0, p.wait_ns);
+        if (ok) {
+          tc_fence_after();
+          for (int h = 0; h < 2; ++h) {
+            issue_s(0, 0, h);
+            mma_commit(B.s_full + 2 * t + h);
+          }
+          mma_commit(B.k_empty + 0);
+          if (seg_hi - u == 1) mma_commit(B.q_empty + 0);
+        }
+      }
+      while (ok && u < u_hi) {
+        const int64_t item = u / nkt;
+        const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
+        const int n_here = (int)(seg_hi - u);
+        const bool final_seg = seg_hi == u_hi;
+        const int n_next = final_seg ? 0 : (int)(min(u_hi, seg_hi + nkt) - seg_hi);
+        const int qb_n = (sg + 1) % C::QB;
+        const uint32_t qp_n = (uint32_t)((sg + 1) / C::QB) & 1u;
+        for (int i = 0; i < n_here; ++i, ++L) {
+          const uint32_t st = L % C::ST, ph = (L / C::ST) & 1u;
+          const uint32_t st1 = (L + 1) % C::ST, ph1 = ((L + 1) / C::ST) & 1u;
+          const bool boundary = i + 1 == n_here;  // tile L + 1 opens the next segment
+          const bool more = !(boundary && final_seg);
+          // tile L + 1 is the last of its segment: its S products release the Q buffer
+          const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
+          const int qb1 = boundary ? qb_n : sg % C::QB;
+          auto next_s = [&](int h) -> bool {
+            if (!mbar_wait(B.k_full + st1, ph1, p.wait_ns) ||
+                (boundary && h == 0 && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n, p.wait_ns)))
+              return false;
+            tc_fence_after();
+            issue_s(qb1, st1, h);
+            mma_commit(B.s_full + 2 * t + h);
+            if (h == 1) {
+              mma_commit(B.k_empty + st1);
+              if (next_last) mma_commit(B.q_empty + qb1);
+            }
+            return true;
+          };
+          if (!mbar_wait(B.v_full + st, ph, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t g = 2 * L + (uint32_t)h;  // compute tile
+            // one barrier per score buffer: S(g + 2) follows PV(g), which
+            // follows this wait, so neither barrier of the buffer can run
+            // two phases ahead of its waiter (a parity wait tells apart
+            // only the current and the previous phase)
+            if (!mbar_wait(B.p_full + 2 * t + h, (g >> 1) & 1u, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(st, h, i > 0 || h > 0);
+            mma_commit(B.o_done + t);
+            if (h == 1) mma_commit(B.v_empty + st);
+            if (more && !boundary && !next_s(h)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          if (more && boundary && !(next_s(0) && next_s(1))) {
+            ok = false;
+            break;
+          }
+        }
+        u = seg_hi;
+        ++sg;
+      }
+      if (!ok) fail_wait(B);
+      mma_commit(B.mma_final + t);
+      mbar_wait(B.mma_final + t, 0, p.wait_ns);
+    }
+  } else if (C::ISS == 2 && C::SUBS == 1 && (wid == C::WI || wid == C::WI + 1)) {
     // ------------------------------------------------------------ MMA issuers (d = 64):
     // one thread per query tile t, for S_t = Q_t K^T and O_t += P_t V.
     // S_t(g+1) goes out as soon as the softmax has read S_t(g) (s_free) and
@@ -644,17 +789,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     // Warp w: query tile t, half hf of each row's columns, TMEM lanes
     // 32 (w mod 4) .. +31 (a warp reaches only its own quarter of the lanes).
     constexpr int HV = C::HV;
-    constexpr int NC = BN / HV;   // score columns of this thread's row
+    constexpr int NC = C::NCOL / HV;  // score columns of this thread's row per compute tile
+    static_assert(C::SUBS == 1 || HV == 1, "64-key compute tiles take one thread per row");
     constexpr int DC = D / HV;    // O columns of this thread's row
     const int t = wid / (4 * HV);
     const int hf = (wid / 4) % HV;
     const int r = (wid & 3) * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((wid & 3) * 32) << 16;
-    const uint32_t tS = tmem + (uint32_t)(t * 128 + hf * NC) + lane_base;
+    // scores of a compute tile: group t's S region, this half's columns, and
+    // with 64-key compute tiles the buffer of the tile's parity
+    const uint32_t tS0 = tmem + (uint32_t)t * C::S_STRIDE + (uint32_t)(hf * NC) + lane_base;
     const uint32_t tO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE + (uint32_t)(hf * DC) + lane_base;
     // packed bf16 probabilities: own columns (EARLY) or over the scores
-    const uint32_t tP = (C::EARLY ? tmem + 256u + (uint32_t)(t * 64) : tmem + (uint32_t)(t * 128)) +
-                        (uint32_t)(hf * NC / 2) + lane_base;
+    const uint32_t tP0 = (C::EARLY ? tmem + 256u + (uint32_t)(t * 64) : tmem + (uint32_t)t * C::S_STRIDE) +
+                         (uint32_t)(hf * NC / 2) + lane_base;
     // 32 columns of this row's O
     auto load_o = [&](int c, float(&tmp)[32]) {
       tmem_ld32(tO + (uint32_t)(c * 32), tmp);
@@ -699,8 +847,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_arrive(B.q_ready + 2 * qb + t);
       float m_run = -INFINITY, l_run = 0.f;
       // ---- the item's key tiles
-      for (int kt = k0; kt < k1; ++kt, ++g) {
-        if (!mbar_wait(B.s_full + t, (uint32_t)g & 1u, p.wait_ns)) {
+      for (int kt = k0; kt < k1 && ok; ++kt) {
+       int key0, nvalid_t;
+       key_tile(p, nt0, kt, key0, nvalid_t);
+       for (int hs = 0; hs < C::SUBS; ++hs, ++g) {
+        const uint32_t buf = C::SUBS == 2 ? (uint32_t)((g & 1) * C::NCOL) : 0u;
+        const uint32_t tS = tS0 + buf;
+        const uint32_t tP = tP0 + (C::EARLY ? 0u : buf);
+        const int nvalid = min(max(nvalid_t - hs * C::NCOL, 0), C::NCOL);
+        const bool first_tile = kt == k0 && hs == 0;
+        // with 64-key compute tiles each score buffer has its own barriers
+        const int sb = C::SUBS == 2 ? 2 * t + (g & 1) : t;
+        const uint32_t sph = C::SUBS == 2 ? (uint32_t)(g >> 1) & 1u : (uint32_t)g & 1u;
+        if (!mbar_wait(B.s_full + sb, sph, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -716,9 +875,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tc_fence_before();
           mbar_arrive(B.s_free + t);
         }
-        int key0, nvalid;
-        key_tile(p, nt0, kt, key0, nvalid);
-        if (nvalid < BN) {
+        if (nvalid < C::NCOL) {
 #pragma unroll
           for (int c = 0; c < NC; ++c)
             sv[c >> 5][c & 31] = (hf * NC + c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
@@ -855,7 +1012,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           ok = false;
           break;
         }
-        if (kt == k0) {
+        if (first_tile) {
           // first tile of the item: its own max first
           m_new = row_max(xgood);
           if (!xgood || !take_turn()) {
@@ -901,14 +1058,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(B.p_full + t);
+        mbar_arrive(B.p_full + sb);
         l_run = l_run * alpha + lsum;
         m_run = m_new;
+       }
       }
       const int g_last = g - 1;
       if (!ok) break;
-      // ---- end of the item's segment: O is complete once the last PV lands
-      if (!mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
+      // ---- end of the item's segment: O is complete once the last PV lands.
+      // With 64-key compute tiles the last scores followed PV(g_last - 2)
+      // only, so o_done may still be two phases short; a parity wait tells
+      // apart only the current and the previous phase, so PV(g_last - 1) is
+      // waited for first.
+      if ((C::SUBS == 2 && g_last >= 1 &&
+           !mbar_wait(B.o_done + t, (uint32_t)(g_last - 1) & 1u, p.wait_ns)) ||
+          !mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
         ok = false;
         break;
       }

@@ -27,6 +27,10 @@ def _bf(rng, shape, scale=1.0):
     (2, 257, 1000, 3, 128),    # several tiles, ragged tails, two problems
     (1, 37, 5, 1, 128),        # fewer keys than one tile
     (1, 384, 4096, 2, 64),     # many key tiles (online-softmax rescaling)
+    (1, 1, 1, 1, 128),         # d = 128 degenerate
+    (1, 300, 130, 2, 128),     # last key tile: 2 keys, its second 64-key half empty
+    (1, 256, 192, 1, 128),     # last key tile: exactly 64 keys
+    (1, 384, 4096, 2, 128),    # d = 128, many key tiles
 ])
 def test_raw_attention_matches_oracle(S, Lq, Lk, H, d):
     rng = np.random.default_rng(1000 + Lq + Lk)
@@ -43,12 +47,13 @@ def test_raw_attention_matches_oracle(S, Lq, Lk, H, d):
         assert err <= TOL, (s, err)
 
 
-def test_raw_attention_large_scores_stay_finite():
+@pytest.mark.parametrize("d", [64, 128])
+def test_raw_attention_large_scores_stay_finite(d):
     """Peaked softmax (scores ~ +-100): the running max must keep exp2 in range."""
     rng = np.random.default_rng(7)
-    S, Lq, Lk, H, d = 1, 128, 640, 1, 64
-    q = _bf(rng, (S, Lq, H, d), 6.0)
-    k = _bf(rng, (S, Lk, H, d), 6.0)
+    S, Lq, Lk, H = 1, 128, 640, 1
+    q = _bf(rng, (S, Lq, H, d), 6.0 * (64 / d) ** 0.25)
+    k = _bf(rng, (S, Lk, H, d), 6.0 * (64 / d) ** 0.25)
     v = _bf(rng, (S, Lk, H, d))
     o = torch.empty((S, Lq, H, d), dtype=torch.bfloat16, device="cuda")
     B.sds_attention(bf16_dev(q), bf16_dev(k), bf16_dev(v), o, S, Lq, Lk, H, d)

@@ -171,6 +171,13 @@ def test_c1_split_key_schedule_with_sink_fill():
     run_sequence(w, 6)
 
 
+def test_c1_d128_split_key_schedule_with_sink_fill():
+    """The same at head_dim 128 (64-key compute tiles, one MMA issuer per
+    query tile) on the persistent split schedule."""
+    w = W.get_config("c1_tiny", d=128, M=2, T=3, R=6, mot_k=3, emb_step=0.5, attn_ctas=5)
+    run_sequence(w, 6)
+
+
 @pytest.mark.parametrize("cfg_type,update_kind,n", [(2, 0, 2), (2, 1, 4), (1, 1, 3), (0, 1, 2)])
 def test_guidance_and_update_variants(cfg_type, update_kind, n):
     """Onetime-negative R-CFG (supplied negative prediction), the strided DDPM
