@@ -28,13 +28,11 @@
 // once P_t(g) is written, so the next scores are ready when the softmax
 // finishes the current tile.  Group t writes P_t(g) only after PV_t(g-1)
 // has completed; it waits for that halfway through its exponentials,
-// holding the first half of P in registers.  The exponentials of the two
-// groups take turns on each SM sub-partition: warp w of group 0 and warp
-// w + 4 of group 1 share one, and hand the turn to each other pair by pair,
-// so each runs alone on its sub-partition's exponential unit while the
-// other loads its scores and takes its row max.  At an item boundary
-// PV_t(g) is issued before S_t(g+1), because the next item's queries are
-// rotated by the softmax only once it has finished the current item.
+// holding the first half of P in registers.  Issuer t releases the K stage
+// of tile g together with its V stage, after PV_t(g) (see the overflow case
+// below).  At an item boundary PV_t(g) is issued before S_t(g+1), because
+// the next item's queries are rotated by the softmax only once it has
+// finished the current item.
 // d = 128.  Each loaded key tile is consumed as two 64-key compute tiles.
 // Tensor memory per group t: two score buffers [t*256, +64), [t*256 + 64,
 // +64) and O_t [t*256 + 128, +128).  P_t(g) is written over the first 32
@@ -48,12 +46,25 @@
 // In both cases the waits for K/V data, which the producer lands several
 // tiles ahead, are taken before the wait for P so they stay off the
 // critical path.
-// The online softmax keeps a running max m per row and rescales O (in
-// tensor memory) only when a tile raises m by more than 8 (log2 units):
-// otherwise probabilities may exceed 1 by up to 2^8, which fp32 sums and
-// bf16 P hold without loss.  Each tile's row max is taken first (a
-// three-input max); the exponentials go against the running max unless the
-// tile raises it past the threshold.  Score scaling and row sums use packed
+// The online softmax keeps a reference m per row (O and the row sum l are
+// kept relative to 2^m) and rescales O in tensor memory when m moves.
+// d = 128: m is the running maximum; each tile's row maximum is taken
+// first (a three-input max) and m moves only when a tile raises it by more
+// than 8 (log2 units), so probabilities stay below 2^8, which fp32 sums and
+// bf16 P hold without loss.
+// d = 64: after an item's first tile (maximum first, m = maximum + 64) the
+// exponentials go against m with no tile maximum at all: taking it costs
+// as much ALU time as the exponentials leave free.  Probabilities are >= 0,
+// so a row sum <= 2^8 bounds every one of them, and in the usual case that
+// is all there is to check.  A larger finite sum (a row's scores rose more
+// than about 64 above its earlier maximum) moves m up by a whole k: the
+// row's largest stored P gives k, and P, the sum and O are multiplied by the
+// exact power of two 2^-k.  An infinite sum (a rise of 192 or more: exp2
+// overflowed) redoes the tile maximum first from scores recomputed on the
+// CUDA cores from Q and K in shared memory; K(g) is still there because its
+// stage is released only after PV(g).  Offsetting m by 64 above the
+// maximum only drops probabilities below 2^-62 of the row's largest.
+// Score scaling and row sums use packed
 // f32x2 arithmetic, halving their instruction count.  Every wait has a time
 // limit (the launch's wait_ns); on expiry the kernel records
 // kErrAttnWaitTimeout in the error word of every stream and leaves.
@@ -75,6 +86,10 @@ constexpr int BM = 128;         // query rows per tile (two tiles per item)
 constexpr int BN = 128;         // keys per tile
 constexpr int SUB = 128 * 128;  // bytes of one 128-row x 64-column bf16 sub-tile
 constexpr float kRescaleThreshold = 8.0f;
+// d = 64: exponentials against the running maximum plus kRefShift (log2
+// units); a row sum above kRowSumLimit moves the reference (see the header).
+constexpr int kRefShift = 64;
+constexpr float kRowSumLimit = 256.0f;
 
 template <int D>
 struct Cfg {
@@ -127,9 +142,6 @@ struct Cfg {
 #ifndef SDS_K1_HV64
 #define SDS_K1_HV64 1
 #endif
-#ifndef SDS_K1_TURNS
-#define SDS_K1_TURNS 2
-#endif
 #ifndef SDS_K1_PWAIT_FIRST
 #define SDS_K1_PWAIT_FIRST 0
 #endif
@@ -167,6 +179,11 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// The two bf16 halves of w as floats (low half first); exact.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -186,11 +203,9 @@ struct Bars {
   uint64_t* o_done;  // [2]
   uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
-  uint64_t* tok;        // [2]: group t has finished its exponentials of a tile (EARLY, HV 1)
   uint64_t* xb;         // [2 tile][2 parity]: both halves' row maxima are in shared memory (HV 2)
   uint64_t* lb;         // [2 tile]: both halves' row sums are in shared memory (HV 2)
   uint64_t* wb;         // [2 tile]: both halves' partial O rows are written (HV 2, split items)
-  uint64_t* tokw;       // [2 group][2 half][4 sub-partition]: per-warp turns at the exponentials
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   float* xmax;          // [2 parity][2 tile][2 half][128]
@@ -214,12 +229,10 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.o_done = r.p_full + 4;
   r.mma_final = r.o_done + 2;
   r.s_free = r.mma_final + 2;
-  r.tok = r.s_free + 2;
-  r.xb = r.tok + 2;
+  r.xb = r.s_free + 2;
   r.lb = r.xb + 4;
   r.wb = r.lb + 2;
-  r.tokw = r.wb + 2;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(r.tokw + 16);
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.wb + 2);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   r.xmax = reinterpret_cast<float*>(sm + C::XCH);
   r.xsum = r.xmax + 8 * 128;
@@ -249,6 +262,49 @@ __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, uint64
   for (int i = 0; i < 1024; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, limit_ns);
+}
+
+// d = 64, one thread per query row, the rare case of the running reference:
+// the exponentials of a key tile overflowed (the row's scores rose 192 or
+// more above its reference).  The tile again, its maximum first, from
+// scores recomputed on the CUDA cores from the query row and the 128 keys
+// in shared memory (64-column bf16 tiles, 128-byte swizzle); P is stored
+// over the overflowed one.  Each score is computed twice (maximum, then
+// probability), so that no score row is held in registers.  Returns the
+// new reference, the factor that takes O and l to it, and the row sum.
+__device__ __noinline__ float3 redo_tile_d64(const uint8_t* qrow, const uint8_t* ks, int r, int nvalid,
+                                             uint32_t tP, float sc, float m_run, float shift) {
+  auto score = [&](int j) -> float {
+    float a = 0.f;
+#pragma unroll 4
+    for (int cw = 0; cw < 32; ++cw) {
+      const uint32_t off = (uint32_t)((cw & 3) * 4);
+      const float2 qf = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(qrow + swz(r, cw >> 2) + off));
+      const float2 kf = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(ks + swz(j, cw >> 2) + off));
+      a = fmaf(qf.y, kf.y, fmaf(qf.x, kf.x, a));
+    }
+    return a;
+  };
+  float mt = -INFINITY;
+#pragma unroll 1
+  for (int j = 0; j < nvalid; ++j) mt = fmaxf(mt, score(j));
+  const float m_new = fmaxf(mt * sc + shift, m_run);
+  float ls = 0.f;
+#pragma unroll 1
+  for (int part = 0; part < 4; ++part) {
+    uint32_t w[16];
+#pragma unroll 1
+    for (int q = 0; q < 16; ++q) {
+      const int j = part * 32 + 2 * q;
+      const float e0 = j < nvalid ? fast_exp2(score(j) * sc - m_new) : 0.f;
+      const float e1 = j + 1 < nvalid ? fast_exp2(score(j + 1) * sc - m_new) : 0.f;
+      ls += e0 + e1;
+      w[q] = pack_bf16x2(e0, e1);
+    }
+    tmem_st16u(tP + (uint32_t)(part * 16), w);
+  }
+  tmem_wait_st();
+  return make_float3(m_new, fast_exp2(m_run - m_new), ls);
 }
 
 // The even division of U units over G CTAs: CTA c owns [lo(c), lo(c+1)).
@@ -353,13 +409,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(B.o_done + i, 1);
       mbar_init(B.mma_final + i, 1);
       mbar_init(B.s_free + i, 128 * C::HV);
-      mbar_init(B.tok + i, 128 * C::HV);
       mbar_init(B.xb + 2 * i + 0, 128 * C::HV);
       mbar_init(B.xb + 2 * i + 1, 128 * C::HV);
       mbar_init(B.lb + i, 128 * C::HV);
       mbar_init(B.wb + i, 128 * C::HV);
     }
-    for (int i = 0; i < 16; ++i) mbar_init(B.tokw + i, 32);
     *B.abort_flag = 0;
     fence_barrier_init();
   }
@@ -605,7 +659,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tc_fence_after();
           issue_s(0, 0);
           mma_commit(B.s_full + t);
-          mma_commit(B.k_empty + 0);
           if (seg_hi - u == 1) mma_commit(B.q_empty + 0);
         }
       }
@@ -635,7 +688,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             tc_fence_after();
             issue_s(qb1, st1);
             mma_commit(B.s_full + t);
-            mma_commit(B.k_empty + st1);
             if (next_last) mma_commit(B.q_empty + qb1);
             return true;
           };
@@ -650,6 +702,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tc_fence_after();
           issue_pv(st, i > 0);
           mma_commit(B.o_done + t);
+          // K(g) is released with V(g), once P_t(g) exists: until then the
+          // softmax may recompute the tile's scores from it
+          mma_commit(B.k_empty + st);
           mma_commit(B.v_empty + st);
           if (more && (boundary || C::PV_FIRST) && !next_s()) {
             ok = false;
@@ -792,6 +847,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     constexpr int NC = C::NCOL / HV;  // score columns of this thread's row per compute tile
     static_assert(C::SUBS == 1 || HV == 1, "64-key compute tiles take one thread per row");
     constexpr int DC = D / HV;    // O columns of this thread's row
+    // d = 64 with one thread per row: after an item's first tile the
+    // exponentials go against the running reference, without a tile maximum
+    constexpr bool RUNREF = C::EARLY && HV == 1;
+    constexpr float kRef = RUNREF ? (float)kRefShift : 0.f;
     const int t = wid / (4 * HV);
     const int hf = (wid / 4) % HV;
     const int r = (wid & 3) * 32 + lane;  // row within the tile == TMEM lane
@@ -859,30 +918,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // with 64-key compute tiles each score buffer has its own barriers
         const int sb = C::SUBS == 2 ? 2 * t + (g & 1) : t;
         const uint32_t sph = C::SUBS == 2 ? (uint32_t)(g >> 1) & 1u : (uint32_t)g & 1u;
-        if (!mbar_wait(B.s_full + sb, sph, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         float sv[NC / 32][32];
-#pragma unroll
-        for (int c = 0; c < NC / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < NC / 32; ++c) reg_fence32(sv[c]);
-        if (C::EARLY) {
-          // the scores are in registers: the issuer may overwrite them
-          tc_fence_before();
-          mbar_arrive(B.s_free + t);
-        }
-        if (nvalid < C::NCOL) {
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-            sv[c >> 5][c & 31] = (hf * NC + c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
-        }
-        // P = exp2(s*sc - m) as packed bf16, stored as it is made over the
-        // first half of this thread's S columns (or, EARLY, P_t's own
-        // columns); returns the sum of this thread's probabilities.
         // EARLY: P_t(g) may overwrite P_t(g-1) only once PV_t(g-1) has read it
         auto p_free = [&]() -> bool {
           if (!C::EARLY || g == 0) return true;
@@ -890,55 +926,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tc_fence_after();
           return true;
         };
-        constexpr int NPART = NC / 32;         // 16 packed columns per part
-        // EARLY: P_t(g) may overwrite P_t(g-1) once PV_t(g-1) has read it.
-        // PWAIT_FIRST waits for that before the exponentials (while the
-        // other group may hold the MUFU turn), so the exponentials never
-        // stall and P is stored as it is made; otherwise the first half of
-        // P waits in registers and the wait falls in the middle.
+        constexpr int NPART = NC / 32;  // 16 packed columns per part
+        // PWAIT_FIRST waits for PV_t(g-1) before the exponentials, so P is
+        // stored as it is made; otherwise the first half of P waits in
+        // registers and the wait falls in the middle of the pass.
         constexpr bool PWAIT_FIRST = C::EARLY && SDS_K1_PWAIT_FIRST;
         constexpr int HOLD = (C::EARLY && !PWAIT_FIRST) ? NPART / 2 : 0;  // parts held until P is free
-        // SDS_K1_TURNS 2: the turn passes between the two warps that share
-        // an SM sub-partition (warp w of group 0 and warp w + 4 of group 1),
-        // each pair on its own, since each sub-partition has its own
-        // exponential unit.  SDS_K1_TURNS 3: the same, with each warp's
-        // exponentials in two halves around its wait for PV(g-1), so that
-        // the other warp's half runs on the unit during that wait
-        // (G0 first, G1 first, G0 second, G1 second, then the next tile).
-        constexpr bool TURNS = C::EARLY && SDS_K1_TURNS;
-        constexpr bool WTURNS = TURNS && SDS_K1_TURNS >= 2 && HV == 1;
-        constexpr bool HTURNS = WTURNS && SDS_K1_TURNS == 3 && HOLD > 0;
-        const int sp4 = wid & 3;
-        // barrier of group tt, half hh, this sub-partition
-        auto tokw = [&](int tt, int hh) { return B.tokw + (tt * 2 + hh) * 4 + sp4; };
-        auto take_half = [&](int hh) -> bool {
-          if (t == 0) {
-            if (hh == 0) return g == 0 || wait_spin(tokw(1, 1), (uint32_t)(g - 1) & 1u, p.wait_ns);
-            return wait_spin(tokw(1, 0), (uint32_t)g & 1u, p.wait_ns);
-          }
-          return wait_spin(tokw(0, hh), (uint32_t)g & 1u, p.wait_ns);
-        };
-        auto take_turn = [&]() -> bool {
-          if (!TURNS) return true;
-          if (HTURNS) return take_half(0);
-          if (WTURNS) {
-            if (t == 0) return g == 0 || wait_spin(tokw(1, 0), (uint32_t)(g - 1) & 1u, p.wait_ns);
-            return wait_spin(tokw(0, 0), (uint32_t)g & 1u, p.wait_ns);
-          }
-          if (t == 0) return g == 0 || wait_spin(B.tok + 1, (uint32_t)(g - 1) & 1u, p.wait_ns);
-          return wait_spin(B.tok + 0, (uint32_t)g & 1u, p.wait_ns);
-        };
-        auto give_turn = [&]() {
-          if (HTURNS) {
-            mbar_arrive(tokw(t, 1));
-          } else if (WTURNS) {
-            mbar_arrive(tokw(t, 0));
-          } else if (TURNS) {
-            mbar_arrive(B.tok + t);
-          }
-        };
         uint32_t pk[NPART][16];
         bool pwait_ok = true;
+        // P = exp2(s*sc - m) as packed bf16, stored as it is made over the
+        // first half of this thread's S columns (or, EARLY, P_t's own
+        // columns); returns the sum of this thread's probabilities.
         auto exp_pass = [&](float m) -> float {
           const float2 nm2 = make_float2(-m, -m);
           constexpr int NRS = SDS_K1_CHAINS;  // independent row-sum chains
@@ -957,9 +955,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             }
             if (part >= HOLD) tmem_st16u(tP + (uint32_t)(part * 16), pk[part]);
             if (HOLD > 0 && part == HOLD - 1) {
-              if (HTURNS) mbar_arrive(tokw(t, 0));  // first half done: the partner's turn
               pwait_ok = p_free();
-              if (HTURNS) pwait_ok = take_half(1) && pwait_ok;
 #pragma unroll
               for (int h = 0; h < HOLD; ++h) tmem_st16u(tP + (uint32_t)(h * 16), pk[h]);
             }
@@ -970,10 +966,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             for (int i = 0; i < w2; ++i) rs[i] = __fadd2_rn(rs[i], rs[i + w2]);
           return rs[0].x + rs[0].y;
         };
-        float alpha = 1.f, m_new, lsum;
-        // EARLY with one thread per row: the two groups take turns at the
-        // exponentials (E0(g), E1(g), E0(g+1), ...), so each runs alone on
-        // the MUFU pipe while the other loads scores and takes its row max
         // this row's maximum score of the tile, times the scale; with two
         // halves, each publishes its own and takes the larger of the two
         auto row_max = [&](bool& good) -> float {
@@ -1007,34 +999,105 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           }
           return m * sc;
         };
+        // RUNREF, a row sum above 2^8 (finite): the row's largest
+        // probability from the stored P (non-negative bf16, so the bit
+        // patterns order like the values), then P, the row sum and, through
+        // alpha, O scaled by the power of two 2^-k that takes it below
+        // 2^-kRefShift again; the reference moves up by k.
+        auto rebase = [&](bool big, float& ls, float& al, float& mn) {
+          tmem_wait_st();
+          uint32_t pmax = 0;
+#pragma unroll
+          for (int h = 0; h < NPART; ++h) {
+            uint32_t w[16];
+            tmem_ld16u(tP + (uint32_t)(h * 16), w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 16; ++q) pmax = max(pmax, max(w[q] >> 16, w[q] & 0xffffu));
+          }
+          // pmax < 2^(e - 126) for the biased exponent e; one multiply by a
+          // normal power of two goes down at most 126 binary orders
+          const int e = (int)(pmax >> 7);
+          const int k = big ? min(max(e - 126 + kRefShift, 0), 126) : 0;
+          const float scale = __int_as_float((127 - k) << 23);
+          const uint32_t s2 = pack_bf16x2(scale, scale);
+#pragma unroll
+          for (int h = 0; h < NPART; ++h) {
+            uint32_t w[16];
+            tmem_ld16u(tP + (uint32_t)(h * 16), w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 16; ++q) w[q] = mul_bf16x2(w[q], s2);
+            tmem_st16u(tP + (uint32_t)(h * 16), w);
+          }
+          ls *= scale;
+          al = scale;
+          mn = m_run + (float)k;
+        };
+        float alpha = 1.f, m_new = m_run, lsum = 0.f;
         bool rescale = false, xgood = true;
+        if (!mbar_wait(B.s_full + sb, sph, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) tmem_ld32(tS + (uint32_t)(c * 32), sv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) reg_fence32(sv[c]);
+        if (C::EARLY) {
+          // the scores are in registers: the issuer may overwrite them
+          tc_fence_before();
+          mbar_arrive(B.s_free + t);
+        }
+        if (nvalid < C::NCOL) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            sv[c >> 5][c & 31] = (hf * NC + c < nvalid) ? sv[c >> 5][c & 31] : -INFINITY;
+        }
         if (PWAIT_FIRST && !p_free()) {
           ok = false;
           break;
         }
-        if (first_tile) {
-          // first tile of the item: its own max first
-          m_new = row_max(xgood);
-          if (!xgood || !take_turn()) {
-            ok = false;
-            break;
+        // the reference of this pass: RUNREF after an item's first tile,
+        // the running one (no tile maximum); otherwise the tile maximum first
+        const bool run = RUNREF && !first_tile;
+        if (!run) {
+          const float mt = row_max(xgood) + kRef;
+          if (first_tile) {
+            m_new = mt;
+          } else {
+            const bool need = mt > m_run + kRescaleThreshold;
+            m_new = need ? mt : m_run;
+            alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+            rescale = __any_sync(0xffffffffu, need);
           }
-          lsum = exp_pass(m_new);
-          give_turn();
-        } else {
-          const float mt = row_max(xgood);
-          const bool need = mt > m_run + kRescaleThreshold;
-          m_new = need ? mt : m_run;
-          alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-          if (!xgood || !take_turn()) {
-            ok = false;
-            break;
-          }
-          lsum = exp_pass(m_new);
-          give_turn();
-          rescale = __any_sync(0xffffffffu, need);
         }
-        if (!pwait_ok) {
+        lsum = exp_pass(m_new);
+        if (run) {
+          // every probability is >= 0, so a row sum <= 2^8 bounds each of them
+          const bool big = !(lsum <= kRowSumLimit);
+          if (__any_sync(0xffffffffu, big)) {
+            if (__any_sync(0xffffffffu, !(lsum < INFINITY))) {
+              // exp2 overflowed: the tile again, maximum first (out of line)
+              tmem_wait_st();
+              if constexpr (RUNREF) {
+                const float3 rr = redo_tile_d64(sQ + (size_t)((sg % C::QB) * 2 + t) * C::TILE,
+                                                sK + (size_t)(g % C::ST) * C::TILE, r, nvalid, tP, sc,
+                                                m_run, kRef);
+                m_new = rr.x;
+                alpha = rr.y;
+                lsum = rr.z;
+              }
+            } else {
+              rebase(big, lsum, alpha, m_new);
+            }
+            rescale = __any_sync(0xffffffffu, alpha != 1.f);
+          }
+        }
+        if (!ok) break;
+        if (!pwait_ok || !xgood) {
           ok = false;
           break;
         }

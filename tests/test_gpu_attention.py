@@ -47,6 +47,63 @@ def test_raw_attention_matches_oracle(S, Lq, Lk, H, d):
         assert err <= TOL, (s, err)
 
 
+def _rising_case(rng, S, Lq, Lk, H, d, ramp):
+    """Queries and keys that share one direction u, with the keys' weight on
+    u growing along the key index: every row's scores climb (ramp > 0) or
+    fall (ramp < 0) across the keys, so the running maximum keeps moving up
+    inside key tiles, not only at their first keys."""
+    u = rng.standard_normal(d)
+    w = np.linspace(0.0, 1.0, Lk) * ramp
+    q = rng.standard_normal((S, Lq, H, d)) + 1.5 * u
+    k = rng.standard_normal((S, Lk, H, d)) + w[None, :, None, None] * u
+    v = rng.standard_normal((S, Lk, H, d))
+    return [W.to_bf16_bits(a.astype(np.float32)) for a in (q, k, v)]
+
+
+def _mid_tile_jumps(q, k, d):
+    """Rows x 32-key parts (not the first part of a 128-key tile) at which
+    the part's largest score, in log2 units, exceeds the largest of all
+    earlier keys by more than 8."""
+    qf = W.bf16_bits_to_f32(q).astype(np.float64)
+    kf = W.bf16_bits_to_f32(k).astype(np.float64)
+    s = np.einsum("qhd,khd->hqk", qf, kf) / np.sqrt(d) / np.log(2.0)
+    Lk = s.shape[-1]
+    n = 0
+    for p0 in range(32, Lk, 32):
+        if p0 % 128 == 0:
+            continue
+        before = s[..., :p0].max(axis=-1)
+        part = s[..., p0:p0 + 32].max(axis=-1)
+        n += int(np.sum(part > before + 8.0))
+    return n
+
+
+@pytest.mark.parametrize("S,Lq,Lk,H,d,ramp", [
+    (1, 512, 1024, 2, 64, 6.0),
+    (1, 256, 640, 1, 64, 20.0),
+    (2, 384, 2048, 1, 64, 12.0),
+    (1, 256, 1000, 1, 64, -6.0),
+    (1, 256, 640, 1, 64, 80.0),    # jumps past the reference overflow exp2: recomputed
+    (1, 300, 700, 1, 64, 200.0),   # ragged, every later tile overflows
+    (1, 256, 1024, 1, 128, 12.0),
+])
+def test_raw_attention_scores_rising_along_the_keys(S, Lq, Lk, H, d, ramp):
+    """The online softmax's reference maximum moves inside key tiles; the
+    probabilities already made against the old reference must follow it."""
+    rng = np.random.default_rng(int(500 + Lq + Lk + 10 * abs(ramp)))
+    q, k, v = _rising_case(rng, S, Lq, Lk, H, d, ramp)
+    if ramp > 0:
+        assert _mid_tile_jumps(q[0], k[0], d) > 0  # the case exercises mid-tile moves
+    o = torch.empty((S, Lq, H, d), dtype=torch.bfloat16, device="cuda")
+    B.sds_attention(bf16_dev(q), bf16_dev(k), bf16_dev(v), o, S, Lq, Lk, H, d)
+    torch.cuda.synchronize()
+    got = W.bf16_bits_to_f32(bf16_host(o)).astype(np.float64)
+    for s in range(S):
+        ref = O.attention(q[s], k[s], v[s])
+        err = attn_rel_err(got[s], ref)
+        assert err <= TOL, (s, err)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_raw_attention_large_scores_stay_finite(d):
     """Peaked softmax (scores ~ +-100): the running max must keep exp2 in range."""
