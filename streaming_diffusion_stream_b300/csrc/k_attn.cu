@@ -1176,80 +1176,94 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // partial: publish (O, m, l) of this row, count in, and merge if last
         const int64_t slot = (item == u_lo / nkt) ? 0 : 1;
         const int64_t rec = ((cta * 2 + slot) * 2 + t) * BM + r;
-        float* wo = p.ws_o + rec * D + hf * DC;
+        const int64_t c_first = sp.owner(item * nkt), c_last = sp.owner((item + 1) * nkt - 1);
+        unsigned int* cnt = p.ws_cnt + (c_first * 2 + t) * BM + r;
+        const unsigned int others = (unsigned int)(c_last - c_first);
+        // One thread per row: when every other contributor has already
+        // counted in, this one is the last and merges straight from its
+        // tensor memory, without publishing its own partial.
+        bool last = HV == 1 && ld_acquire_u32(cnt) == others;
+        if (!last) {
+          float* wo = p.ws_o + rec * D + hf * DC;
 #pragma unroll
-        for (int c = 0; c < DC / 32; ++c) {
-          float tmp[32];
-          load_o(c, tmp);
+          for (int c = 0; c < DC / 32; ++c) {
+            float tmp[32];
+            load_o(c, tmp);
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
-            __stcg(reinterpret_cast<float4*>(wo + c * 32 + q),
-                   make_float4(tmp[q], tmp[q + 1], tmp[q + 2], tmp[q + 3]));
-        }
-        if (hf == 0) __stcg(p.ws_ml + rec, make_float2(m_run, l_run));
-        __threadfence();
-        if (HV == 2) {
-          // the row's other half is written too before it is counted
-          mbar_arrive(B.wb + t);
-          if (!mbar_wait(B.wb + t, (uint32_t)nsplit & 1u, p.wait_ns)) {
-            ok = false;
-            break;
+            for (int q = 0; q < 32; q += 4)
+              __stcg(reinterpret_cast<float4*>(wo + c * 32 + q),
+                     make_float4(tmp[q], tmp[q + 1], tmp[q + 2], tmp[q + 3]));
           }
-          ++nsplit;
-          __threadfence();
-        }
-        if (hf == 0) {
-          const int64_t c_first = sp.owner(item * nkt), c_last = sp.owner((item + 1) * nkt - 1);
-          unsigned int* cnt = p.ws_cnt + (c_first * 2 + t) * BM + r;
-          const unsigned int prev = atomicAdd(cnt, 1u);
-          if (prev == (unsigned int)(c_last - c_first)) {
+          if (hf == 0) __stcg(p.ws_ml + rec, make_float2(m_run, l_run));
+          if (HV == 2) {
+            // the row's other half is written too before it is counted
             __threadfence();
-            float M = -INFINITY;
-            for (int64_t cc = c_first; cc <= c_last; ++cc) {
-              const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-              M = fmaxf(M, __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r).x);
+            mbar_arrive(B.wb + t);
+            if (!mbar_wait(B.wb + t, (uint32_t)nsplit & 1u, p.wait_ns)) {
+              ok = false;
+              break;
             }
-            float Lsum = 0.f;
-            for (int64_t cc = c_first; cc <= c_last; ++cc) {
-              const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-              const float2 ml = __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r);
-              Lsum += ml.y * fast_exp2(ml.x - M);
-            }
-            const float inv = 1.f / Lsum;
-            uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
+            ++nsplit;
+          }
+          // release: this row's partial is visible before the count;
+          // acquire: the last arriver sees every other partial
+          if (hf == 0) last = atomic_add_acq_rel_u32(cnt, 1u) == others;
+        }
+        if (last && hf == 0) {
+          // the others' records; this CTA's own (m, l) and, with one thread
+          // per row, its O come from registers and tensor memory
+          const bool own_here = HV == 1;
+          float M = m_run, Lsum = l_run;
+          for (int64_t cc = c_first; cc <= c_last; ++cc) {
+            if (cc == cta) continue;
+            const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+            const float2 ml = __ldcg(p.ws_ml + ((cc * 2 + sl) * 2 + t) * BM + r);
+            const float Mn = fmaxf(M, ml.x);
+            Lsum = Lsum * fast_exp2(M - Mn) + ml.y * fast_exp2(ml.x - Mn);
+            M = Mn;
+          }
+          const float inv = 1.f / Lsum;
+          const float w_own = fast_exp2(m_run - M) * inv;
+          uint16_t* orow = p.o + (((int64_t)ip.s * p.q_rows + row) * p.H + ip.h) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              float acc[32];
+          for (int c = 0; c < D / 32; ++c) {
+            float acc[32];
+            if (own_here) {
+              load_o(c, acc);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) acc[q] *= w_own;
+            } else {
 #pragma unroll
               for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-              for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
-                const int64_t rc = ((cc * 2 + sl) * 2 + t) * BM + r;
-                const float w = fast_exp2(__ldcg(p.ws_ml + rc).x - M) * inv;
-                const float4* src = reinterpret_cast<const float4*>(p.ws_o + rc * D + c * 32);
+            }
+            for (int64_t cc = c_first; cc <= c_last; ++cc) {
+              if (cc == cta && own_here) continue;
+              const int64_t sl = (item == sp.lo(cc) / nkt) ? 0 : 1;
+              const int64_t rc = ((cc * 2 + sl) * 2 + t) * BM + r;
+              const float w = fast_exp2(__ldcg(p.ws_ml + rc).x - M) * inv;
+              const float4* src = reinterpret_cast<const float4*>(p.ws_o + rc * D + c * 32);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 v = __ldcg(src + q);
-                  acc[4 * q + 0] = __fmaf_rn(v.x, w, acc[4 * q + 0]);
-                  acc[4 * q + 1] = __fmaf_rn(v.y, w, acc[4 * q + 1]);
-                  acc[4 * q + 2] = __fmaf_rn(v.z, w, acc[4 * q + 2]);
-                  acc[4 * q + 3] = __fmaf_rn(v.w, w, acc[4 * q + 3]);
-                }
-              }
-              if (row < p.q_rows) {
-#pragma unroll
-                for (int q = 0; q < 32; q += 8) {
-                  uint4 pk;
-                  pk.x = pack_bf16x2(acc[q + 0], acc[q + 1]);
-                  pk.y = pack_bf16x2(acc[q + 2], acc[q + 3]);
-                  pk.z = pack_bf16x2(acc[q + 4], acc[q + 5]);
-                  pk.w = pack_bf16x2(acc[q + 6], acc[q + 7]);
-                  *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
-                }
+              for (int q = 0; q < 8; ++q) {
+                const float4 v = __ldcg(src + q);
+                acc[4 * q + 0] = __fmaf_rn(v.x, w, acc[4 * q + 0]);
+                acc[4 * q + 1] = __fmaf_rn(v.y, w, acc[4 * q + 1]);
+                acc[4 * q + 2] = __fmaf_rn(v.z, w, acc[4 * q + 2]);
+                acc[4 * q + 3] = __fmaf_rn(v.w, w, acc[4 * q + 3]);
               }
             }
-            *cnt = 0u;  // ready for the next launch
+            if (row < p.q_rows) {
+#pragma unroll
+              for (int q = 0; q < 32; q += 8) {
+                uint4 pk;
+                pk.x = pack_bf16x2(acc[q + 0], acc[q + 1]);
+                pk.y = pack_bf16x2(acc[q + 2], acc[q + 3]);
+                pk.z = pack_bf16x2(acc[q + 4], acc[q + 5]);
+                pk.w = pack_bf16x2(acc[q + 6], acc[q + 7]);
+                *reinterpret_cast<uint4*>(orow + c * 32 + q) = pk;
+              }
+            }
           }
+          *cnt = 0u;  // ready for the next launch
         }
       }
     }
