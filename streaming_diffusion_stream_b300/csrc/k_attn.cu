@@ -27,8 +27,8 @@
 // as soon as group t has read S_t(g) into registers (s_free), then PV_t(g)
 // once P_t(g) is written, so the next scores are ready when the softmax
 // finishes the current tile.  Group t writes P_t(g) only after PV_t(g-1)
-// has completed; it waits for that halfway through its exponentials,
-// holding the first half of P in registers.  Issuer t releases the K stage
+// has completed; it waits for that three quarters of the way through its
+// exponentials, holding those parts of P in registers.  Issuer t releases the K stage
 // of tile g together with its V stage, after PV_t(g) (see the overflow case
 // below).  At an item boundary PV_t(g) is issued before S_t(g+1), because
 // the next item's queries are rotated by the softmax only once it has
@@ -456,7 +456,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           issued_k = g + 1;
         }
         if (do_v) {
-          if (!mbar_wait(B.v_empty + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
+          // d = 64 releases K(g) and V(g) together, on k_empty alone
+          if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
           mbar_arrive_expect_tx(B.v_full + st, C::TILE);
           for (int b = 0; b < C::NSUB; ++b)
             tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
@@ -702,10 +703,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tc_fence_after();
           issue_pv(st, i > 0);
           mma_commit(B.o_done + t);
-          // K(g) is released with V(g), once P_t(g) exists: until then the
-          // softmax may recompute the tile's scores from it
+          // K(g) and V(g) are released together (one commit on k_empty),
+          // once P_t(g) exists: until then the softmax may recompute the
+          // tile's scores from K(g)
           mma_commit(B.k_empty + st);
-          mma_commit(B.v_empty + st);
           if (more && (boundary || C::PV_FIRST) && !next_s()) {
             ok = false;
             break;
@@ -928,10 +929,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         };
         constexpr int NPART = NC / 32;  // 16 packed columns per part
         // PWAIT_FIRST waits for PV_t(g-1) before the exponentials, so P is
-        // stored as it is made; otherwise the first half of P waits in
-        // registers and the wait falls in the middle of the pass.
+        // stored as it is made; otherwise the first three quarters of P wait
+        // in registers and the wait falls late in the pass.
         constexpr bool PWAIT_FIRST = C::EARLY && SDS_K1_PWAIT_FIRST;
-        constexpr int HOLD = (C::EARLY && !PWAIT_FIRST) ? NPART / 2 : 0;  // parts held until P is free
+        constexpr int HOLD = (C::EARLY && !PWAIT_FIRST) ? 3 * NPART / 4 : 0;  // parts held until P is free
         uint32_t pk[NPART][16];
         bool pwait_ok = true;
         // P = exp2(s*sc - m) as packed bf16, stored as it is made over the
