@@ -104,6 +104,28 @@ def test_raw_attention_scores_rising_along_the_keys(S, Lq, Lk, H, d, ramp):
         assert err <= TOL, (s, err)
 
 
+@pytest.mark.parametrize("ctas,ramp", [
+    (37, 20.0),    # 2-3 key tiles per CTA: later tiles move the reference (stored P rescaled)
+    (37, 80.0),    # ... or overflow and are recomputed
+    (160, 80.0),   # single-tile contributors: every partial starts from its own maximum
+])
+def test_split_key_schedule_with_rising_scores(ctas, ramp):
+    """Items split between CTAs whose contributors ended on different
+    references (some moved inside their key range) merge to the oracle's
+    result."""
+    w = W.get_config("c2_sdturbo_image", L=320, H=2, grid_h=16, grid_w=20, latent_h=16, latent_w=20,
+                     ssf_h=64, ssf_w=64, attn_ctas=ctas)
+    rng = np.random.default_rng(int(900 + ctas + ramp))
+    q, k, v = _rising_case(rng, w["streams"], w["q_rows"], w["kv_rows"], w["H"], w["d"], ramp)
+    g = GpuPipe(w)
+    try:
+        for rep in range(2):  # the second launch reuses the arrival counters
+            got = g.attend(q, k, v)
+            assert attn_rel_err(got[0], O.attention(q[0], k[0], v[0])) <= TOL, rep
+    finally:
+        g.close()
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_raw_attention_large_scores_stay_finite(d):
     """Peaked softmax (scores ~ +-100): the running max must keep exp2 in range."""
