@@ -597,7 +597,12 @@ static sds_status attend_common(sds_ctx* ctx, const CUtensorMap& tq, const CUten
     ap.wait_ns = kAttnWaitNs;
     ap.withhold_k = -1;
   }
-  cudaError_t e = launch_attention(tq, tk, tv, ap, head_dim, S, sm_count, st);
+  CUtensorMap to;
+  if (!make_tmap_bf16(&to, ap.o, (int64_t)ap.H * head_dim, ap.q_rows, S)) {
+    if (ctx) return fail(ctx, SDS_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed for o");
+    return fail(nullptr, SDS_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed for o");
+  }
+  cudaError_t e = launch_attention(tq, tk, tv, to, ap, head_dim, S, sm_count, st);
   if (e != cudaSuccess) {
     if (ctx) return cuda_fail(ctx, e, "attention launch");
     return fail(nullptr, SDS_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));

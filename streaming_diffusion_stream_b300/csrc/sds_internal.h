@@ -76,10 +76,12 @@ inline size_t attn_ws_bytes(int d) {
   return (size_t)kAttnMaxCtas * 2 * 2 * 128 * ((size_t)d * 4 + 8) + (size_t)kAttnMaxCtas * 2 * 128 * 4;
 }
 
-// q/k/v tensor maps: 3-D {H*d, rows, S}, box {64, 128, 1}, 128-byte swizzle.
+// q/k/v/o tensor maps: 3-D {H*d, rows, S}, box {64, 128, 1}, 128-byte swizzle.
+// to: the output o as the same kind of map (written by TMA at the end of a
+// CTA's last item).
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int head_dim, int S, int sm_count,
-                             cudaStream_t st);
+                             const CUtensorMap& to, const AttnParams& p, int head_dim, int S,
+                             int sm_count, cudaStream_t st);
 
 // Build a bf16 3-D tensor map {H*d, rows, S} with a {64, 128, 1} box.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t hd, int64_t rows, int64_t S);
