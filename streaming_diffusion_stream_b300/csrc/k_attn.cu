@@ -896,9 +896,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const int seg[3] = {p.rope_seg[0], p.rope_seg[1], p.rope_seg[2]};
         const int off[3] = {p.tab_off[0], p.tab_off[1], p.tab_off[2]};
         uint8_t* qt = sQ + (qb * 2 + t) * C::TILE;
-        // this half's share of the row's 16-byte chunks (8 per 64 columns)
+        // this half's share of the row's 16-byte chunks (8 per 64 columns);
+        // four chunks at a time keep 16 table loads in flight (1 % of the
+        // c4 launch against two at a time)
         constexpr int CH = C::NSUB * 8 / HV;
-#pragma unroll 2
+#pragma unroll 4
         for (int k = hf * CH; k < (hf + 1) * CH; ++k) {
           const int b = k >> 3, c = k & 7;
           uint4* ptr = reinterpret_cast<uint4*>(qt + b * SUB + swz(r, c));
