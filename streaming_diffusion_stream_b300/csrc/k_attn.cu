@@ -259,6 +259,7 @@ __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, uint64_t 
   return mbar_wait(bar, parity, limit_ns);
 }
 __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
   for (int i = 0; i < 1024; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, limit_ns);
