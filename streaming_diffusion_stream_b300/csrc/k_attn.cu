@@ -40,9 +40,12 @@
 // into the same buffer (one thread's MMAs run in issue order, so the PV
 // reads P before the S overwrites it), keeping the scores of the next
 // compute tile ready while the softmax works on the current one.  Each
-// score buffer has its own s_full / p_full barriers, so that no barrier can
-// run two phases ahead of its waiter (a parity wait distinguishes only the
-// current and the previous phase).
+// score buffer has its own s_full / p_full / o_done barriers, so that no
+// barrier can run two phases ahead of its waiter (a parity wait
+// distinguishes only the current and the previous phase).  The issuer
+// signals o_done only for the last key tile of an item's segment, and the
+// commit that releases K(L + 1) also releases V(L): three commits per key
+// tile instead of six (about 1 % of the launch at c4).
 // In both cases the waits for K/V data, which the producer lands several
 // tiles ahead, are taken before the wait for P so they stay off the
 // critical path.
@@ -104,7 +107,7 @@ struct Cfg {
   // work; two threads issuing concurrently reach the full rate).
   // Layout S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
   // O0 [384,448) O1 [448,512).  d = 128 has no spare columns: P overwrites
-  // the first 64 columns of its S and one thread issues every MMA.
+  // the first columns of its score buffer.
   static constexpr bool EARLY = (D == 64);
 #ifndef SDS_K1_ISS128
 #define SDS_K1_ISS128 1
@@ -200,7 +203,7 @@ struct Bars {
   uint64_t* v_empty;
   uint64_t* s_full;  // [2 group][2 buffer]: index t, or t * 2 + buffer with 64-key compute tiles
   uint64_t* p_full;  // [2 group][2 buffer], indexed as s_full
-  uint64_t* o_done;  // [2]
+  uint64_t* o_done;  // [2 group][2 buffer]: index t, or t * 2 + buffer with 64-key compute tiles
   uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
   uint64_t* xb;         // [2 tile][2 parity]: both halves' row maxima are in shared memory (HV 2)
@@ -227,7 +230,7 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.s_full = r.v_empty + C::ST;
   r.p_full = r.s_full + 4;
   r.o_done = r.p_full + 4;
-  r.mma_final = r.o_done + 2;
+  r.mma_final = r.o_done + 4;
   r.s_free = r.mma_final + 2;
   r.xb = r.s_free + 2;
   r.lb = r.xb + 4;
@@ -407,9 +410,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int i = 0; i < 4; ++i) {
       mbar_init(B.s_full + i, 1);
       mbar_init(B.p_full + i, 128 * C::HV);
+      mbar_init(B.o_done + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(B.o_done + i, 1);
       mbar_init(B.mma_final + i, 1);
       mbar_init(B.s_free + i, 128 * C::HV);
       mbar_init(B.xb + 2 * i + 0, 128 * C::HV);
@@ -459,8 +462,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           issued_k = g + 1;
         }
         if (do_v) {
-          // d = 64 releases K(g) and V(g) together, on k_empty alone
-          if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) { ok = false; break; }
+          // d = 64 releases K(g) and V(g) together, on k_empty alone; with
+          // 64-key compute tiles the commit that releases K(g + 1) also
+          // releases V(g) (it follows PV(g) in issue order)
+          if (C::SUBS == 2) {
+            if (g >= C::ST && !mbar_wait(B.k_empty + (g - 1) % C::ST, (uint32_t)((g - 1) / C::ST) & 1u, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+          } else if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(B.v_full + st, C::TILE);
           for (int b = 0; b < C::NSUB; ++b)
             tma_load_3d(sV + st * C::TILE + b * SUB, &tm_v, ip.h * D + b * 64, key0, ip.s, B.v_full + st);
@@ -598,8 +611,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             }
             tc_fence_after();
             issue_pv(st, h, i > 0 || h > 0);
-            mma_commit(B.o_done + t);
-            if (h == 1) mma_commit(B.v_empty + st);
+            // O is read by the softmax only at the end of a segment (and for
+            // a rescale, which otherwise waits for S(g + 1), issued after PV(g - 1))
+            if (boundary) mma_commit(B.o_done + 2 * t + h);
             if (more && !boundary && !next_s(h)) {
               ok = false;
               break;
@@ -1110,8 +1124,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           break;
         }
         if (rescale) {
-          // O may be rescaled only once the previous PV into it has landed
-          if (!mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u, p.wait_ns)) {
+          // O may be rescaled only once the previous PV into it has landed.
+          // With 64-key compute tiles the issuer signals o_done only for a
+          // segment's last key tile; elsewhere the scores of tile g + 1,
+          // issued after PV(g - 1), show that PV(g - 1) has landed.
+          const bool seg_last = kt + 1 == k1 && hs + 1 == C::SUBS;
+          const bool landed =
+              C::SUBS == 2 ? (seg_last ? mbar_wait(B.o_done + 2 * t, (uint32_t)sg & 1u, p.wait_ns)
+                                       : mbar_wait(B.s_full + 2 * t + ((g + 1) & 1),
+                                                   (uint32_t)((g + 1) >> 1) & 1u, p.wait_ns))
+                           : mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u, p.wait_ns);
+          if (!landed) {
             ok = false;
             break;
           }
@@ -1142,14 +1165,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       const int g_last = g - 1;
       if (!ok) break;
-      // ---- end of the item's segment: O is complete once the last PV lands.
-      // With 64-key compute tiles the last scores followed PV(g_last - 2)
-      // only, so o_done may still be two phases short; a parity wait tells
-      // apart only the current and the previous phase, so PV(g_last - 1) is
-      // waited for first.
-      if ((C::SUBS == 2 && g_last >= 1 &&
-           !mbar_wait(B.o_done + t, (uint32_t)(g_last - 1) & 1u, p.wait_ns)) ||
-          !mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
+      // ---- end of the item's segment: O is complete once the last PV lands
+      // (with 64-key compute tiles: the PV of each half of the segment's last
+      // key tile, one o_done phase per segment)
+      if (C::SUBS == 2 ? (!mbar_wait(B.o_done + 2 * t, (uint32_t)sg & 1u, p.wait_ns) ||
+                          !mbar_wait(B.o_done + 2 * t + 1, (uint32_t)sg & 1u, p.wait_ns))
+                       : !mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
         ok = false;
         break;
       }
