@@ -104,18 +104,22 @@ def test_raw_attention_scores_rising_along_the_keys(S, Lq, Lk, H, d, ramp):
         assert err <= TOL, (s, err)
 
 
-@pytest.mark.parametrize("ctas,ramp", [
-    (37, 20.0),    # 2-3 key tiles per CTA: later tiles move the reference (stored P rescaled)
-    (37, 80.0),    # ... or overflow and are recomputed
-    (160, 80.0),   # single-tile contributors: every partial starts from its own maximum
+@pytest.mark.parametrize("ctas,ramp,d", [
+    (37, 20.0, 64),    # 2-3 key tiles per CTA: later tiles move the reference (stored P rescaled)
+    (37, 80.0, 64),    # ... or overflow and are recomputed
+    (160, 80.0, 64),   # single-tile contributors: every partial starts from its own maximum
+    # d = 128: O is rescaled at most tiles, inside segments (after the next
+    # tile's scores) and at a segment's last tile (after its o_done)
+    (37, 20.0, 128),
+    (160, 20.0, 128),  # one key tile per segment: its last tile is also its first
 ])
-def test_split_key_schedule_with_rising_scores(ctas, ramp):
+def test_split_key_schedule_with_rising_scores(ctas, ramp, d):
     """Items split between CTAs whose contributors ended on different
     references (some moved inside their key range) merge to the oracle's
     result."""
-    w = W.get_config("c2_sdturbo_image", L=320, H=2, grid_h=16, grid_w=20, latent_h=16, latent_w=20,
+    w = W.get_config("c2_sdturbo_image", L=320, H=2, d=d, grid_h=16, grid_w=20, latent_h=16, latent_w=20,
                      ssf_h=64, ssf_w=64, attn_ctas=ctas)
-    rng = np.random.default_rng(int(900 + ctas + ramp))
+    rng = np.random.default_rng(int(900 + ctas + ramp + (d - 64)))
     q, k, v = _rising_case(rng, w["streams"], w["q_rows"], w["kv_rows"], w["H"], w["d"], ramp)
     g = GpuPipe(w)
     try:
