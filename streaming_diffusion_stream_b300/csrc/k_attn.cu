@@ -22,6 +22,8 @@
 //   warps 4-7  softmax group 1 (tile Q1)
 //   warp  8    TMA producer: K and V tiles of 128 keys through an ST-stage ring, Q per item
 //   warps 9-10 MMA issuers (one thread each): issuer t serves query tile t
+//              (d = 128: its S products only)
+//   warp  11   d = 128 only: the PV products of both query tiles
 // d = 64.  Tensor memory (512 columns): S0, S1 (128 each, fp32 scores),
 // P0, P1 (64 each, packed bf16), O0, O1 (64 each).  Issuer t issues S_t(g+1)
 // as soon as group t has read S_t(g) into registers (s_free), then PV_t(g)
@@ -36,16 +38,15 @@
 // d = 128.  Each loaded key tile is consumed as two 64-key compute tiles.
 // Tensor memory per group t: two score buffers [t*256, +64), [t*256 + 64,
 // +64) and O_t [t*256 + 128, +128).  P_t(g) is written over the first 32
-// columns of its score buffer; issuer t issues PV_t(g) and then S_t(g+2)
-// into the same buffer (one thread's MMAs run in issue order, so the PV
-// reads P before the S overwrites it), keeping the scores of the next
-// compute tile ready while the softmax works on the current one.  Each
-// score buffer has its own s_full / p_full / o_done barriers, so that no
-// barrier can run two phases ahead of its waiter (a parity wait
-// distinguishes only the current and the previous phase).  The issuer
-// signals o_done only for the last key tile of an item's segment, and the
-// commit that releases K(L + 1) also releases V(L): three commits per key
-// tile instead of six (about 1 % of the launch at c4).
+// columns of its score buffer.  The MMA stream bounds d = 128 (an issuing
+// thread needs 72-78 cycles per MMA, and the S products run at N = 64), so
+// it is spread over three warps: warp 9 + t issues S_t, warp 11 issues PV
+// for both tiles.  S_t(g+2) goes into the buffer of S_t(g) once PV_t(g)
+// has completed (an o_done barrier per buffer), keeping the scores of the
+// next compute tile ready while the softmax works on the current one.
+// Each score buffer has its own s_full / p_full / o_done barriers, so that
+// no barrier can run two phases ahead of its waiter (a parity wait
+// distinguishes only the current and the previous phase).
 // In both cases the waits for K/V data, which the producer lands several
 // tiles ahead, are taken before the wait for P so they stay off the
 // critical path.
@@ -124,11 +125,10 @@ struct Cfg {
   // d = 128 with 64-key compute tiles (SUBS = 2): each loaded 128-key tile
   // is consumed as two 64-key halves.  Tensor memory then holds two score
   // buffers per group, [t*256, +64) and [t*256 + 64, +64), beside O_t at
-  // [t*256 + 128, +128): the issuer of group t computes S_t(g+2) into the
-  // buffer of S_t(g) right after PV_t(g) has read the P written over it,
-  // so the scores of the next half-tile are ready while the softmax works
-  // on the current one, and the group's tensor work never waits for its
-  // own softmax.
+  // [t*256 + 128, +128): the S issuer of group t computes S_t(g+2) into
+  // the buffer of S_t(g) once PV_t(g), issued by the PV warp, has read the
+  // P written over it, so the scores of the next half-tile are ready while
+  // the softmax works on the current one.
   static constexpr int SUBS = (D == 128 && SDS_K1_SUB64) ? 2 : 1;
   static constexpr int NCOL = BN / SUBS;  // keys per compute tile
   static constexpr int ISS = (EARLY || SUBS == 2) ? 2 : SDS_K1_ISS128;
@@ -167,7 +167,12 @@ struct Cfg {
   static constexpr int WP = SMW;                  // TMA producer warp (K, Q; and V unless SPLITV)
   static constexpr int WI = SMW + 1;              // MMA issuer warp(s): WI, WI + 1
   static constexpr int WPV = SMW + 3;             // V producer warp (SPLITV)
-  static constexpr int THREADS = (SMW + (SPLITV ? 4 : 3)) * 32;
+  // d = 128 (64-key compute tiles): warps WI, WI + 1 issue the S products of
+  // tiles 0 and 1, warp WPVI the PV products of both
+  static constexpr bool PVW = SUBS == 2;
+  static constexpr int WPVI = SMW + 3;
+  static_assert(!(PVW && SPLITV), "the PV issuer warp and the V producer warp are the same warp");
+  static constexpr int THREADS = (SMW + ((SPLITV || PVW) ? 4 : 3)) * 32;
   static constexpr int Q = 0;
   static constexpr int K = Q + QB * 2 * TILE;
   static constexpr int V = K + ST * TILE;
@@ -204,7 +209,7 @@ struct Bars {
   uint64_t* s_full;  // [2 group][2 buffer]: index t, or t * 2 + buffer with 64-key compute tiles
   uint64_t* p_full;  // [2 group][2 buffer], indexed as s_full
   uint64_t* o_done;  // [2 group][2 buffer]: index t, or t * 2 + buffer with 64-key compute tiles
-  uint64_t* mma_final;  // [2]: per issuing thread (warp 9, warp 10)
+  uint64_t* mma_final;  // [3]: per issuing thread (warps 9, 10 and, d = 128, 11)
   uint64_t* s_free;     // [2]: the softmax has read S_t (EARLY)
   uint64_t* xb;         // [2 tile][2 parity]: both halves' row maxima are in shared memory (HV 2)
   uint64_t* lb;         // [2 tile]: both halves' row sums are in shared memory (HV 2)
@@ -231,7 +236,7 @@ __device__ __forceinline__ Bars carve(uint8_t* sm) {
   r.p_full = r.s_full + 4;
   r.o_done = r.p_full + 4;
   r.mma_final = r.o_done + 4;
-  r.s_free = r.mma_final + 2;
+  r.s_free = r.mma_final + 3;
   r.xb = r.s_free + 2;
   r.lb = r.xb + 4;
   r.wb = r.lb + 2;
@@ -405,13 +410,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(B.k_full + i, 1);
       mbar_init(B.v_full + i, 1);
       mbar_init(B.k_empty + i, C::ISS);
-      mbar_init(B.v_empty + i, C::ISS);
+      mbar_init(B.v_empty + i, C::PVW ? 1 : C::ISS);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(B.s_full + i, 1);
       mbar_init(B.p_full + i, 128 * C::HV);
       mbar_init(B.o_done + i, 1);
     }
+    mbar_init(B.mma_final + 2, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.mma_final + i, 1);
       mbar_init(B.s_free + i, 128 * C::HV);
@@ -465,12 +471,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           // d = 64 releases K(g) and V(g) together, on k_empty alone; with
           // 64-key compute tiles the commit that releases K(g + 1) also
           // releases V(g) (it follows PV(g) in issue order)
-          if (C::SUBS == 2) {
-            if (g >= C::ST && !mbar_wait(B.k_empty + (g - 1) % C::ST, (uint32_t)((g - 1) / C::ST) & 1u, p.wait_ns)) {
-              ok = false;
-              break;
-            }
-          } else if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) {
+          if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -505,43 +506,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int64_t j = (issued_v > C::ST ? issued_v - C::ST : 0); j < issued_v; ++j)
         mbar_wait(B.v_full + j % C::ST, (uint32_t)(j / C::ST) & 1u, p.wait_ns);
     }
-  } else if (C::SUBS == 2 && (wid == C::WI || wid == C::WI + 1)) {
+  } else if (C::SUBS == 2 && (wid == C::WI || wid == C::WI + 1 || wid == C::WPVI)) {
     // ------------------------------------------------------------ MMA issuers (d = 128,
-    // 64-key compute tiles): issuer t serves query tile t.  The two halves
-    // h of a loaded key tile have score buffers of their own; once PV_t(g)
-    // has been issued, S_t(g + 2) goes into the same buffer (one thread's
-    // MMAs run in issue order, so PV_t(g) reads the P written over the
-    // scores before S_t(g + 2) overwrites them).  At an item boundary the
-    // next item's two S products follow the item's last PV, because the
-    // softmax rotates the next item's queries only once it has finished
-    // the item.
+    // 64-key compute tiles).  Warp WI + t issues the S products of query
+    // tile t; warp WPVI issues the PV products of both tiles.  (One thread
+    // issuing both for its tile spent most of a step issuing, at 72-78
+    // cycles per MMA; two lanes of one warp do not issue concurrently.)
+    // The two halves h of a loaded key tile have score buffers of their
+    // own, and P is written over the scores, so S_t(L + 1, h) waits until
+    // PV_t(L, h) has completed (one o_done barrier per buffer).  At an item
+    // boundary the next item's S products also wait for its queries, which
+    // the softmax rotates once it has finished the item.
     if (lane == 0 && active) {
-      const int t = wid - C::WI;
+      const bool s_role = wid != C::WPVI;
+      const int ts = wid - C::WI;  // the S issuer's tile
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, C::NCOL, false);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);
       const uint32_t dhi = (uint32_t)(smem_desc_sw128(0, 0, 1024) >> 32);
       const uint32_t qlo = (uint32_t)smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t klo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint32_t vlo = (uint32_t)smem_desc_sw128(smem_u32(sV), SUB, 1024);
-      const uint32_t dS = tmem + (uint32_t)t * C::S_STRIDE;  // buffer h at dS + h * NCOL
-      const uint32_t dO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE;
       // S_t of half h of the K tile in stage st: keys [h * NCOL, +NCOL) are
       // rows h * NCOL.. of each 64-column sub-tile (a multiple of the 8-row
-      // swizzle atom, so the descriptor only moves its start address)
-      auto issue_s = [&](int qb, uint32_t st, int h) {
+      // swizzle atom, so the descriptor only moves its start address); the
+      // buffer of group t, half h, is at t * S_STRIDE + h * NCOL
+      auto issue_s = [&](int t, int qb, uint32_t st, int h) {
+        const uint32_t dS = tmem + (uint32_t)t * C::S_STRIDE + (uint32_t)(h * C::NCOL);
         const uint32_t a0 = qlo + (uint32_t)(((qb * 2 + t) * C::TILE) >> 4);
         const uint32_t b0 = klo + st * (uint32_t)(C::TILE >> 4) + (uint32_t)((h * C::NCOL * 128) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (uint32_t)(((kk >> 2) * SUB + (kk & 3) * 32) >> 4);
-          mma_bf16_ss_w(dS + (uint32_t)(h * C::NCOL), a0 + off, dhi, b0 + off, dhi, IDESC_S,
-                        kk > 0 ? 1u : 0u);
+          mma_bf16_ss_w(dS, a0 + off, dhi, b0 + off, dhi, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t(half h) V(rows h * NCOL.. of the V tile in stage st)
-      auto issue_pv = [&](uint32_t st, int h, bool acc) {
+      auto issue_pv = [&](int t, uint32_t st, int h, bool acc) {
+        const uint32_t dO = tmem + C::O_COL + (uint32_t)t * C::O_STRIDE;
+        const uint32_t aP = tmem + (uint32_t)t * C::S_STRIDE + (uint32_t)(h * C::NCOL);
         const uint32_t b0 = vlo + st * (uint32_t)(C::TILE >> 4);
-        const uint32_t aP = dS + (uint32_t)(h * C::NCOL);
 #pragma unroll
         for (int kk = 0; kk < C::NCOL / 16; ++kk)
           mma_bf16_ts_w(dO, aP + (uint32_t)(kk * 8),
@@ -552,15 +555,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       uint32_t L = 0;  // loaded key tiles consumed (compute tiles 2L, 2L + 1)
       int sg = 0;      // segment counter
       int64_t u = u_lo;
-      {
+      if (s_role) {
         const int64_t item = u / nkt;
         const int64_t seg_hi = min(u_hi, (item + 1) * nkt);
-        ok = mbar_wait(B.q_ready + t, 0, p.wait_ns) && mbar_wait(B.k_full, 0, p.wait_ns);
+        ok = mbar_wait(B.q_ready + ts, 0, p.wait_ns) && mbar_wait(B.k_full, 0, p.wait_ns);
         if (ok) {
           tc_fence_after();
           for (int h = 0; h < 2; ++h) {
-            issue_s(0, 0, h);
-            mma_commit(B.s_full + 2 * t + h);
+            issue_s(ts, 0, 0, h);
+            mma_commit(B.s_full + 2 * ts + h);
           }
           mma_commit(B.k_empty + 0);
           if (seg_hi - u == 1) mma_commit(B.q_empty + 0);
@@ -574,63 +577,58 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const int n_next = final_seg ? 0 : (int)(min(u_hi, seg_hi + nkt) - seg_hi);
         const int qb_n = (sg + 1) % C::QB;
         const uint32_t qp_n = (uint32_t)((sg + 1) / C::QB) & 1u;
-        for (int i = 0; i < n_here; ++i, ++L) {
+        for (int i = 0; i < n_here && ok; ++i, ++L) {
           const uint32_t st = L % C::ST, ph = (L / C::ST) & 1u;
-          const uint32_t st1 = (L + 1) % C::ST, ph1 = ((L + 1) / C::ST) & 1u;
-          const bool boundary = i + 1 == n_here;  // tile L + 1 opens the next segment
-          const bool more = !(boundary && final_seg);
-          // tile L + 1 is the last of its segment: its S products release the Q buffer
-          const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
-          const int qb1 = boundary ? qb_n : sg % C::QB;
-          auto next_s = [&](int h) -> bool {
+          if (s_role) {
+            const bool boundary = i + 1 == n_here;  // tile L + 1 opens the next segment
+            if (boundary && final_seg) continue;    // no tile L + 1
+            const uint32_t st1 = (L + 1) % C::ST, ph1 = ((L + 1) / C::ST) & 1u;
+            // tile L + 1 is the last of its segment: its S products release the Q buffer
+            const bool next_last = boundary ? n_next == 1 : i + 2 == n_here;
+            const int qb1 = boundary ? qb_n : sg % C::QB;
             if (!mbar_wait(B.k_full + st1, ph1, p.wait_ns) ||
-                (boundary && h == 0 && !mbar_wait(B.q_ready + 2 * qb1 + t, qp_n, p.wait_ns)))
-              return false;
-            tc_fence_after();
-            issue_s(qb1, st1, h);
-            mma_commit(B.s_full + 2 * t + h);
-            if (h == 1) {
-              mma_commit(B.k_empty + st1);
-              if (next_last) mma_commit(B.q_empty + qb1);
-            }
-            return true;
-          };
-          if (!mbar_wait(B.v_full + st, ph, p.wait_ns)) {
-            ok = false;
-            break;
-          }
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t g = 2 * L + (uint32_t)h;  // compute tile
-            // one barrier per score buffer: S(g + 2) follows PV(g), which
-            // follows this wait, so neither barrier of the buffer can run
-            // two phases ahead of its waiter (a parity wait tells apart
-            // only the current and the previous phase)
-            if (!mbar_wait(B.p_full + 2 * t + h, (g >> 1) & 1u, p.wait_ns)) {
+                (boundary && !mbar_wait(B.q_ready + 2 * qb1 + ts, qp_n, p.wait_ns))) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            issue_pv(st, h, i > 0 || h > 0);
-            // O is read by the softmax only at the end of a segment (and for
-            // a rescale, which otherwise waits for S(g + 1), issued after PV(g - 1))
-            if (boundary) mma_commit(B.o_done + 2 * t + h);
-            if (more && !boundary && !next_s(h)) {
+            for (int h = 0; h < 2 && ok; ++h) {
+              // S_t(L + 1, h) goes over the P that PV_t(L, h) reads.  PV_t(L - 1, h)
+              // completed before S_t(L, h) was issued, so the barrier is in
+              // phase L or L + 1 here and the parity wait is exact.
+              ok = mbar_wait(B.o_done + 2 * ts + h, L & 1u, p.wait_ns);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(ts, qb1, st1, h);
+              mma_commit(B.s_full + 2 * ts + h);
+            }
+            if (!ok) break;
+            mma_commit(B.k_empty + st1);
+            if (next_last) mma_commit(B.q_empty + qb1);
+          } else {
+            if (!mbar_wait(B.v_full + st, ph, p.wait_ns)) {
               ok = false;
               break;
             }
-          }
-          if (!ok) break;
-          if (more && boundary && !(next_s(0) && next_s(1))) {
-            ok = false;
-            break;
+            for (int h = 0; h < 2 && ok; ++h) {
+              for (int t = 0; t < 2 && ok; ++t) {
+                ok = mbar_wait(B.p_full + 2 * t + h, L & 1u, p.wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, st, h, i > 0 || h > 0);
+                mma_commit(B.o_done + 2 * t + h);
+              }
+            }
+            if (!ok) break;
+            mma_commit(B.v_empty + st);
           }
         }
         u = seg_hi;
         ++sg;
       }
       if (!ok) fail_wait(B);
-      mma_commit(B.mma_final + t);
-      mbar_wait(B.mma_final + t, 0, p.wait_ns);
+      const int fin = s_role ? ts : 2;
+      mma_commit(B.mma_final + fin);
+      mbar_wait(B.mma_final + fin, 0, p.wait_ns);
     }
   } else if (C::ISS == 2 && C::SUBS == 1 && (wid == C::WI || wid == C::WI + 1)) {
     // ------------------------------------------------------------ MMA issuers (d = 64):
@@ -881,6 +879,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const uint32_t tP0 = (C::EARLY ? tmem + 256u + (uint32_t)(t * 64) : tmem + (uint32_t)t * C::S_STRIDE) +
                          (uint32_t)(hf * NC / 2) + lane_base;
     // 32 columns of this row's O
+    // PV_t of compute tile gg has landed in O.  With 64-key compute tiles
+    // each score buffer has its own o_done barrier, whose phase is the
+    // loaded tile; otherwise o_done counts compute tiles.
+    auto o_landed = [&](int gg) -> bool {
+      const int ob = C::SUBS == 2 ? 2 * t + (gg & 1) : t;
+      const uint32_t par = C::SUBS == 2 ? (uint32_t)(gg >> 1) & 1u : (uint32_t)gg & 1u;
+      return mbar_wait(B.o_done + ob, par, p.wait_ns);
+    };
     auto load_o = [&](int c, float(&tmp)[32]) {
       tmem_ld32(tO + (uint32_t)(c * 32), tmp);
       tmem_wait_ld();
@@ -1124,17 +1130,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           break;
         }
         if (rescale) {
-          // O may be rescaled only once the previous PV into it has landed.
-          // With 64-key compute tiles the issuer signals o_done only for a
-          // segment's last key tile; elsewhere the scores of tile g + 1,
-          // issued after PV(g - 1), show that PV(g - 1) has landed.
-          const bool seg_last = kt + 1 == k1 && hs + 1 == C::SUBS;
-          const bool landed =
-              C::SUBS == 2 ? (seg_last ? mbar_wait(B.o_done + 2 * t, (uint32_t)sg & 1u, p.wait_ns)
-                                       : mbar_wait(B.s_full + 2 * t + ((g + 1) & 1),
-                                                   (uint32_t)((g + 1) >> 1) & 1u, p.wait_ns))
-                           : mbar_wait(B.o_done + t, (uint32_t)(g - 1) & 1u, p.wait_ns);
-          if (!landed) {
+          // O may be rescaled only once the previous PV into it has landed
+          if (!o_landed(g - 1)) {
             ok = false;
             break;
           }
@@ -1166,11 +1163,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const int g_last = g - 1;
       if (!ok) break;
       // ---- end of the item's segment: O is complete once the last PV lands
-      // (with 64-key compute tiles: the PV of each half of the segment's last
-      // key tile, one o_done phase per segment)
-      if (C::SUBS == 2 ? (!mbar_wait(B.o_done + 2 * t, (uint32_t)sg & 1u, p.wait_ns) ||
-                          !mbar_wait(B.o_done + 2 * t + 1, (uint32_t)sg & 1u, p.wait_ns))
-                       : !mbar_wait(B.o_done + t, (uint32_t)g_last & 1u, p.wait_ns)) {
+      // (with 64-key compute tiles, the last PV of each score buffer)
+      if ((C::SUBS == 2 && !o_landed(g_last - 1)) || !o_landed(g_last)) {
         ok = false;
         break;
       }
