@@ -468,9 +468,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           issued_k = g + 1;
         }
         if (do_v) {
-          // d = 64 releases K(g) and V(g) together, on k_empty alone; with
-          // 64-key compute tiles the commit that releases K(g + 1) also
-          // releases V(g) (it follows PV(g) in issue order)
+          // d = 64 releases K(g) and V(g) together, on k_empty alone; d = 128
+          // releases V(g) on v_empty (the PV warp, after PV(g))
           if (!mbar_wait((C::EARLY ? B.k_empty : B.v_empty) + st, ph ^ 1u, p.wait_ns)) {
             ok = false;
             break;
