@@ -395,6 +395,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int64_t u_lo = sp.lo(cta), u_hi = sp.lo(cta + 1);
   const bool active = nkt > 0 && u_hi > u_lo;
 
+  // d = 64: a tile recomputed in the overflow case reads its queries from
+  // shared memory, until the end of its segment.  The producer refills a Q
+  // buffer two segments later, after the K/V copies of the full item in
+  // between, each of which waits for the PV product ST tiles back; with
+  // items of at most ST - 2 key tiles that can happen before the softmax
+  // has finished, so then the softmax threads also arrive on q_empty.
+  const bool q_by_softmax = C::EARLY && nkt <= C::ST - 2;
   if (tid == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (!C::EARLY) prefetch_tensormap(&tm_o);  // o is written by TMA only at d = 128 (a d = 64 prefetch cost 1.5 %)
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.q_full + i, 1);
-      mbar_init(B.q_empty + i, C::ISS);
+      mbar_init(B.q_empty + i, q_by_softmax ? C::ISS + 256 * C::HV : C::ISS);
       mbar_init(B.q_ready + 2 * i + 0, 128 * C::HV);
       mbar_init(B.q_ready + 2 * i + 1, 128 * C::HV);
     }
@@ -1161,6 +1168,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       const int g_last = g - 1;
       if (!ok) break;
+      if (q_by_softmax) {
+        // every tile of the segment is done, including any recomputation
+        // from the queries in shared memory: the Q buffer may be refilled
+        mbar_arrive(B.q_empty + qb);
+      }
       // ---- end of the item's segment: O is complete once the last PV lands
       // (with 64-key compute tiles, the last PV of each score buffer)
       if ((C::SUBS == 2 && !o_landed(g_last - 1)) || !o_landed(g_last)) {

@@ -321,3 +321,250 @@ def test_model_catches_a_missing_query_wait():
         except AssertionError:
             hits += 1
     assert hits > 0
+
+
+# --------------------------------------------------------------------------
+# head_dim 64: one issuing thread per tile (S and PV), P in its own columns,
+# four K/V stages released together after PV, two Q buffers, and the
+# softmax's rare recomputation of a tile's scores from Q and K in shared
+# memory (the overflow case of the running reference).
+
+ST64, QB64 = 4, 2
+
+
+class Sim64(Sim):
+    def __init__(self, seed, u_lo, u_hi, nkt, p_redo=0.3, softmax_frees_q=None):
+        # as the kernel: the softmax arrives on q_empty for items of at most ST - 2 tiles
+        if softmax_frees_q is None:
+            softmax_frees_q = nkt <= ST64 - 2
+        self.rng = random.Random(seed)
+        self.u_lo, self.u_hi, self.nkt = u_lo, u_hi, nkt
+        self.p_redo = p_redo
+        self.softmax_frees_q = softmax_frees_q
+        B = {}
+        for qb in range(QB64):
+            B[f"q_full{qb}"] = Bar(f"q_full{qb}", 1)
+            B[f"q_empty{qb}"] = Bar(f"q_empty{qb}", 2 + (2 if softmax_frees_q else 0))
+            for t in range(2):
+                B[f"q_ready{2 * qb + t}"] = Bar(f"q_ready{2 * qb + t}", 1)
+        for s in range(ST64):
+            B[f"k_full{s}"] = Bar(f"k_full{s}", 1)
+            B[f"v_full{s}"] = Bar(f"v_full{s}", 1)
+            B[f"k_empty{s}"] = Bar(f"k_empty{s}", 2)
+        for t in range(2):
+            for name in ("s_full", "s_free", "p_full", "o_done"):
+                B[f"{name}{t}"] = Bar(f"{name}{t}", 1)
+        self.B = B
+        self.segs = []
+        u = u_lo
+        while u < u_hi:
+            hi = min(u_hi, (u // nkt + 1) * nkt)
+            self.segs.append((u, hi))
+            u = hi
+        self.loaded_k, self.loaded_v, self.stage_k, self.stage_v = {}, {}, {}, {}
+        self.q_buf = {0: -1, 1: -1}      # segment whose queries the buffer holds (from the copy's issue)
+        self.q_landed = set()
+        self.q_rot = {0: -1, 1: -1}
+        self.s_read = set()              # (t, g): the softmax holds S_t(g) in registers
+        self.tile_done = set()           # (t, g): the softmax has finished tile g (P stored, p_full)
+        self.done_ops, self.issued, self.p_written = set(), set(), set()
+        self.epilogue_done = {0: -1, 1: -1}
+        self.queues, self.tma = {}, []
+
+    def producer(self):
+        n = self.u_hi - self.u_lo
+        for g in range(n):
+            st = g % ST64
+            for kind in ("k", "v"):
+                yield ("wait", f"k_empty{st}", g // ST64 - 1)
+                stage = self.stage_k if kind == "k" else self.stage_v
+                old = stage.get(st)
+                if old is not None:
+                    if kind == "k":  # read by the S products and by a recomputation of tile old
+                        assert all(("S", t, old, ) in self.done_ops for t in range(2)), ("K", g)
+                        assert all((t, old) in self.tile_done for t in range(2)), ("K reused", g)
+                        self.loaded_k.pop(old, None)
+                    else:
+                        assert all(("PV", t, old) in self.done_ops for t in range(2)), ("V", g)
+                        self.loaded_v.pop(old, None)
+                stage[st] = g
+                self.tma.append((kind, g, st))
+            sg = self.seg_of(g)
+            if self.u_lo + g == self.segs[sg][0]:
+                qb = sg % QB64
+                if sg >= QB64:
+                    yield ("wait", f"q_empty{qb}", sg // QB64 - 1)
+                    old = sg - QB64
+                    tiles = [g2 for g2 in range(n) if self.seg_of(g2) == old]
+                    assert all(("S", t, g2) in self.done_ops for t in range(2) for g2 in tiles), ("Q", sg)
+                    # a recomputation in segment `old` reads these queries
+                    assert all((t, g2) in self.tile_done for t in range(2) for g2 in tiles), ("Q reused", sg)
+                self.q_buf[qb] = sg
+                self.tma.append(("q", sg, qb))
+
+    def issuer(self, t):
+        th = f"I{t}"
+
+        def issue_s(g, qb):
+            assert g in self.loaded_k, ("S before K", t, g)
+            assert self.q_buf[qb] == self.seg_of(g) and self.q_rot[t] == self.seg_of(g), ("S before Q", t, g)
+            if g >= 1:
+                assert (t, g - 1) in self.s_read, ("S over unread scores", t, g)
+            self.issue(th, ("S", t, g))
+
+        yield ("wait", f"q_ready{t}", 0)
+        yield ("wait", "k_full0", 0)
+        issue_s(0, 0)
+        self.commit(th, f"s_full{t}")
+        if self.segs[0][1] - self.segs[0][0] == 1:
+            self.commit(th, "q_empty0")
+        g = 0
+        for sg, (lo, hi) in enumerate(self.segs):
+            n_here = hi - lo
+            final = sg == len(self.segs) - 1
+            n_next = 0 if final else self.segs[sg + 1][1] - self.segs[sg + 1][0]
+            for i in range(n_here):
+                st, st1 = g % ST64, (g + 1) % ST64
+                boundary = i + 1 == n_here
+                more = not (boundary and final)
+                next_last = n_next == 1 if boundary else i + 2 == n_here
+
+                def next_s():
+                    qb1 = (sg + 1) % QB64 if boundary else sg % QB64
+                    yield ("wait", f"k_full{st1}", (g + 1) // ST64)
+                    yield ("wait", f"s_free{t}", g)
+                    if boundary:
+                        yield ("wait", f"q_ready{2 * qb1 + t}", (sg + 1) // QB64)
+                    issue_s(g + 1, qb1)
+                    self.commit(th, f"s_full{t}")
+                    if next_last:
+                        self.commit(th, f"q_empty{qb1}")
+
+                if more and not boundary:
+                    yield from next_s()
+                yield ("wait", f"v_full{st}", g // ST64)
+                yield ("wait", f"p_full{t}", g)
+                assert (t, g) in self.p_written and g in self.loaded_v, ("PV early", t, g)
+                if i == 0:
+                    assert self.epilogue_done[t] == sg - 1, ("O overwritten", t, sg)
+                self.issue(th, ("PV", t, g))
+                self.commit(th, f"o_done{t}")
+                self.commit(th, f"k_empty{st}")
+                if more and boundary:
+                    yield from next_s()
+                g += 1
+
+    def softmax(self, t):
+        g = 0
+        for sg, (lo, hi) in enumerate(self.segs):
+            qb = sg % QB64
+            yield ("wait", f"q_full{qb}", sg // QB64)
+            assert sg in self.q_landed and self.q_buf[qb] == sg
+            self.q_rot[t] = sg
+            self.B[f"q_ready{2 * qb + t}"].arrive()
+            for i in range(hi - lo):
+                yield ("wait", f"s_full{t}", g)
+                assert ("S", t, g) in self.done_ops, ("scores read early", t, g)
+                self.s_read.add((t, g))
+                self.B[f"s_free{t}"].arrive()
+                if g >= 1:  # P_t(g) goes over P_t(g - 1)
+                    yield ("wait", f"o_done{t}", g - 1)
+                    assert ("PV", t, g - 1) in self.done_ops, ("P over unread P", t, g)
+                self.p_written.add((t, g))
+                if i > 0 and self.rng.random() < self.p_redo:
+                    # the overflow case: this tile's scores again, from the
+                    # queries and keys in shared memory
+                    assert self.q_buf[qb] == sg, ("recomputation read overwritten queries", t, g)
+                    assert self.stage_k.get(g % ST64) == g and g in self.loaded_k, ("recomputation K", t, g)
+                self.tile_done.add((t, g))
+                self.B[f"p_full{t}"].arrive()
+                g += 1
+            if self.softmax_frees_q:
+                self.B[f"q_empty{qb}"].arrive()
+            yield ("wait", f"o_done{t}", g - 1)
+            assert all(("PV", t, g2) in self.done_ops for g2 in range(g)), ("O read early", t, sg)
+            self.epilogue_done[t] = sg
+
+    def run(self, max_steps=200000):
+        agents = [self.producer(), self.issuer(0), self.issuer(1), self.softmax(0), self.softmax(1)]
+        pending = {}
+
+        def advance(i):
+            try:
+                pending[i] = next(agents[i])
+            except StopIteration:
+                pending[i] = "done"
+
+        for i in range(len(agents)):
+            advance(i)
+        for _ in range(max_steps):
+            choices = [("agent", i) for i, w in pending.items() if w != "done" and self.wait_ok(w[1], w[2])]
+            choices += [("thread", th) for th, q in self.queues.items() if q]
+            if self.tma:
+                choices.append(("tma", None))
+            if not choices:
+                break
+            kind, x = self.rng.choice(choices)
+            if kind == "agent":
+                advance(x)
+            elif kind == "thread":
+                what, item = self.queues[x].pop(0)
+                if what == "op":
+                    self.done_ops.add(item)
+                else:
+                    self.B[item].arrive()
+            else:
+                kind2, a, b = self.tma.pop(self.rng.randrange(len(self.tma)))
+                if kind2 == "k":
+                    self.loaded_k[a] = b
+                    self.B[f"k_full{b}"].arrive()
+                elif kind2 == "v":
+                    self.loaded_v[a] = b
+                    self.B[f"v_full{b}"].arrive()
+                else:
+                    self.q_landed.add(a)
+                    self.B[f"q_full{b}"].arrive()
+        stuck = {i: w for i, w in pending.items() if w != "done"}
+        assert not stuck, f"deadlock: {stuck}"
+        assert not any(self.queues.values()) and not self.tma
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_d64_protocol_random_schedules(seed):
+    rng = random.Random(2000 + seed)
+    nkt = rng.choice([1, 2, 3, 5, 8])
+    u_lo = rng.randrange(0, 3 * nkt)
+    u_hi = u_lo + rng.randint(1, 16)
+    Sim64(seed, u_lo, u_hi, nkt, p_redo=rng.choice([0.0, 0.3, 1.0])).run()
+
+
+def test_d64_model_catches_q_refilled_under_a_recomputation():
+    """Without the softmax's own arrival on q_empty, the producer may refill
+    a Q buffer once the S products of the segment two back have completed,
+    while that segment's softmax can still recompute a tile's scores from
+    those queries. This is possible only when segments are shorter than
+    the K/V ring (items of at most three key tiles). The model finds the
+    hazard, so for such items the kernel's softmax arrives on q_empty at
+    the end of each segment; for longer items the copies in between already
+    wait for the softmax, and the model finds no hazard without that
+    arrival."""
+    hits = 0
+    for seed in range(200):
+        rng = random.Random(5000 + seed)
+        nkt = rng.choice([1, 2, 3])
+        u_lo = rng.randrange(0, 3 * nkt)
+        try:
+            Sim64(seed, u_lo, u_lo + rng.randint(4, 12), nkt, p_redo=1.0, softmax_frees_q=False).run()
+        except AssertionError as e:
+            assert "Q reused" in str(e) or "overwritten queries" in str(e), e
+            hits += 1
+    assert hits > 0
+
+
+@pytest.mark.parametrize("nkt", [3, 4, 5, 8])
+def test_d64_longer_items_need_no_softmax_arrival(nkt):
+    for seed in range(80):
+        rng = random.Random(7000 + seed)
+        u_lo = rng.randrange(0, 3 * nkt)
+        Sim64(seed, u_lo, u_lo + rng.randint(1, 4 * nkt + 4), nkt, p_redo=1.0,
+              softmax_frees_q=False).run()
