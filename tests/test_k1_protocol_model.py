@@ -568,3 +568,63 @@ def test_d64_longer_items_need_no_softmax_arrival(nkt):
         u_lo = rng.randrange(0, 3 * nkt)
         Sim64(seed, u_lo, u_lo + rng.randint(1, 4 * nkt + 4), nkt, p_redo=1.0,
               softmax_frees_q=False).run()
+
+
+# --------------------------------------------------------------------------
+# Split items: the contributors of one query row merge through an arrival
+# counter, with no waiting.  Each contributor at the end of its key range
+# (one thread per row):
+# - loads the counter with acquire; if every other contributor has counted
+#   in, it is the last and merges its own O from tensor memory, publishing
+#   nothing;
+# - otherwise it publishes (O, m, l), then adds 1 with acquire-release; if
+#   the old value shows every other contributor counted in, it is the last
+#   and merges.
+# The merger resets the counter for the next launch.
+
+
+def merge_round(rng, n):
+    """One row with n contributors under a random interleaving; returns
+    (mergers, partials the merger could read, counter after the launch)."""
+    cnt = [0]
+    published = set()
+    mergers = []
+    # each contributor's steps as a generator; a step is one atomic action
+    def contributor(c):
+        if cnt[0] == n - 1:  # acquire load: the others have counted in
+            mergers.append((c, set(published), "direct"))
+            cnt[0] = 0
+            return
+        yield
+        published.add(c)      # the partial, then the count (release)
+        yield
+        old = cnt[0]
+        cnt[0] += 1
+        if old == n - 1:
+            yield
+            mergers.append((c, set(published) - {c}, "counted"))
+            cnt[0] = 0
+
+    gens = [contributor(c) for c in range(n)]
+    live = list(range(n))
+    while live:
+        i = rng.choice(live)
+        try:
+            next(gens[i])
+        except StopIteration:
+            live.remove(i)
+    return mergers, cnt[0]
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 7])
+def test_split_item_merge_has_one_merger_that_sees_every_partial(n):
+    rng = random.Random(n)
+    direct = 0
+    for _ in range(400):
+        mergers, cnt = merge_round(rng, n)
+        assert len(mergers) == 1, mergers
+        who, seen, path = mergers[0]
+        assert seen >= set(range(n)) - {who}, (who, seen)
+        assert cnt == 0
+        direct += path == "direct"
+    assert 0 < direct < 400  # both ways of being last occur
